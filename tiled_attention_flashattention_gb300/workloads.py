@@ -1,0 +1,126 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random inputs; it holds none of the attention
+arithmetic, so the CUDA path and the CPU oracle can both take their inputs from
+it.  Every tensor is drawn on the CPU from ``torch.Generator('cpu')`` seeded
+with ``20261202 + index``, as fp32 N(0, 1), then cast to bf16 (round to
+nearest even).  Draw order: Q, K, V for prefill; Q_nope, Q_pe, KV_latent, K_pe
+for MLA decode.
+
+The long-context workload scales 1% of the key rows by 8 before the bf16 cast
+(x8 is exact in bf16): the same ``round(0.01 * N_kv)`` row indices, drawn with
+``randperm`` from the same generator after V, for every (batch, head).  Large
+scores then appear late in a row and force the running maximum to move.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+SEED_BASE = 20261202
+
+
+@dataclass(frozen=True)
+class PrefillCase:
+    name: str
+    B: int
+    H: int
+    H_kv: int
+    N_q: int
+    N_kv: int
+    d: int
+    causal: bool
+    window: int = 0
+    spike_frac: float = 0.0      # fraction of key rows scaled by spike_mult
+    spike_mult: float = 8.0
+    seed: int = SEED_BASE
+    scale: float = field(default=float("nan"))
+
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d) if math.isnan(self.scale) else self.scale
+
+
+@dataclass(frozen=True)
+class MlaCase:
+    name: str
+    B: int
+    H: int
+    N_kv: int
+    d_c: int = 512
+    d_r: int = 64
+    seed: int = SEED_BASE
+    scale: float = field(default=float("nan"))
+
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d_c + self.d_r) if math.isnan(self.scale) else self.scale
+
+
+# The five named workloads (index = seed offset), plus the window variant of
+# the GQA one, which shares its inputs.
+WORKLOADS = {
+    "mha_b1_h2_n128_d64": PrefillCase("mha_b1_h2_n128_d64", 1, 2, 2, 128, 128, 64, False,
+                                      seed=SEED_BASE + 0),
+    "mha_causal_b4_h16_n2048_d128": PrefillCase("mha_causal_b4_h16_n2048_d128", 4, 16, 16, 2048,
+                                                2048, 128, True, seed=SEED_BASE + 1),
+    "gqa_causal_b2_h32_hkv8_n8192_d128": PrefillCase("gqa_causal_b2_h32_hkv8_n8192_d128", 2, 32, 8,
+                                                     8192, 8192, 128, True, seed=SEED_BASE + 2),
+    "gqa_window256_b2_h32_hkv8_n8192_d128": PrefillCase("gqa_window256_b2_h32_hkv8_n8192_d128", 2, 32,
+                                                        8, 8192, 8192, 128, True, window=256,
+                                                        seed=SEED_BASE + 2),
+    "mla_decode_b64_h128_nkv4096": MlaCase("mla_decode_b64_h128_nkv4096", 64, 128, 4096,
+                                           seed=SEED_BASE + 3),
+    "mha_causal_spiky_b1_h32_n16384_d128": PrefillCase("mha_causal_spiky_b1_h32_n16384_d128", 1, 32,
+                                                       32, 16384, 16384, 128, True, spike_frac=0.01,
+                                                       seed=SEED_BASE + 4),
+}
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def prefill_inputs(case: PrefillCase):
+    """(Q, K, V) bf16 CPU tensors: Q [B,H,N_q,d], K/V [B,H_kv,N_kv,d]."""
+    g = _gen(case.seed)
+    Q = torch.randn(case.B, case.H, case.N_q, case.d, generator=g, dtype=torch.float32)
+    K = torch.randn(case.B, case.H_kv, case.N_kv, case.d, generator=g, dtype=torch.float32)
+    V = torch.randn(case.B, case.H_kv, case.N_kv, case.d, generator=g, dtype=torch.float32)
+    if case.spike_frac > 0 and case.N_kv > 0:
+        n_spike = int(round(case.spike_frac * case.N_kv))
+        idx = torch.randperm(case.N_kv, generator=g)[:n_spike]
+        K[:, :, idx, :] *= case.spike_mult
+    return Q.to(torch.bfloat16), K.to(torch.bfloat16), V.to(torch.bfloat16)
+
+
+def mla_inputs(case: MlaCase):
+    """(Q_nope [B,H,d_c], Q_pe [B,H,d_r], KV_latent [B,N_kv,d_c], K_pe [B,N_kv,d_r]) bf16 CPU."""
+    g = _gen(case.seed)
+    Qn = torch.randn(case.B, case.H, case.d_c, generator=g, dtype=torch.float32)
+    Qp = torch.randn(case.B, case.H, case.d_r, generator=g, dtype=torch.float32)
+    KV = torch.randn(case.B, case.N_kv, case.d_c, generator=g, dtype=torch.float32)
+    Kp = torch.randn(case.B, case.N_kv, case.d_r, generator=g, dtype=torch.float32)
+    return tuple(x.to(torch.bfloat16) for x in (Qn, Qp, KV, Kp))
+
+
+def random_prefill(B, H, H_kv, N_q, N_kv, d, seed, dist="normal"):
+    """Small ad-hoc prefill inputs for edge-case tests (same drawing recipe)."""
+    g = _gen(seed)
+    shape_q, shape_kv = (B, H, N_q, d), (B, H_kv, N_kv, d)
+    if dist == "normal":
+        draw = lambda s: torch.randn(*s, generator=g, dtype=torch.float32)
+    elif dist == "int":   # small integers: exactly representable, exact products
+        draw = lambda s: torch.randint(-3, 4, s, generator=g).to(torch.float32)
+    else:
+        raise ValueError(dist)
+    return tuple(draw(s).to(torch.bfloat16) for s in (shape_q, shape_kv, shape_kv))
+
+
+def random_mla(B, H, N_kv, d_c, d_r, seed):
+    g = _gen(seed)
+    shapes = [(B, H, d_c), (B, H, d_r), (B, N_kv, d_c), (B, N_kv, d_r)]
+    return tuple(torch.randn(*s, generator=g, dtype=torch.float32).to(torch.bfloat16)
+                 for s in shapes)
