@@ -1,0 +1,149 @@
+/*
+ * gbattn.h -- C ABI of libgbattn.so: fused attention forward on one GB300
+ * (sm_103a), in two forms.
+ *
+ *  attn_fwd    FlashAttention-style prefill, MHA or GQA, optional causal mask
+ *              and causal sliding window.
+ *  mla_decode  FlashMLA-style decode: one query token per sequence, H query
+ *              heads sharing one latent KV head (d_c = 512) plus a RoPE key
+ *              part (d_r = 64); the values are the latent KV rows themselves.
+ *
+ * Both compute O = softmax(scale * Q K^T + mask) V with an online softmax, so
+ * the score matrix never leaves the chip ("TileLang 学习笔记", section
+ * "FlashAttention 的实现": S = Q K^T, P = softmax(S), O = P V, and the
+ * running max / running sum update of "Online Softmax 的关键").  They also
+ * return LSE, the natural-log log-sum-exp of each row's scaled, masked
+ * scores: LSE_i = ln sum_j exp(scale * q_i . k_j) over the allowed keys j.
+ *
+ * Conventions for every entry point
+ *  - Pointers to tensors are DEVICE pointers on the current CUDA device.  The
+ *    caller allocates and owns every buffer; the library never allocates,
+ *    frees or keeps a reference to them past the call.
+ *  - Tensors are dense, row-major, with no padding.  bf16 is IEEE bfloat16
+ *    (raw 16-bit storage); LSE is fp32.  Tensor base addresses must be 16-byte
+ *    aligned (TMA requirement), else GBATTN_ERR_ALIGNMENT.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they return once the kernels are enqueued.  Arguments are
+ *    validated first; on any error nothing is enqueued and the function
+ *    returns a non-zero gbattn_status, with a message in gbattn_last_error().
+ *  - Every wait inside the kernels is bounded.  A wait that runs out records
+ *    an error in a per-library device status word and the kernel returns
+ *    without finishing; gbattn_check() reports it as GBATTN_ERR_TIMEOUT.
+ *  - Thread safety: calls may come from several host threads; the last-error
+ *    message is per host thread.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GBATTN_OK = 0,
+    GBATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, H % H_kv != 0, ... */
+    GBATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not in {64,128}) */
+    GBATTN_ERR_ALIGNMENT = 3,     /* a tensor base address is not 16-byte aligned */
+    GBATTN_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned */
+    GBATTN_ERR_LAUNCH = 5,        /* CUDA runtime/driver error while preparing or launching */
+    GBATTN_ERR_TIMEOUT = 6,       /* a device-side bounded wait ran out (from gbattn_check) */
+    GBATTN_ERR_ARCH = 7           /* current device is not compute capability 10.3 (sm_103) */
+} gbattn_status;
+
+/*
+ * attn_fwd -- prefill attention forward.
+ *
+ * Operation ("TileLang 学习笔记", FlashAttention 的实现; the score mask is the
+ * additive 0 / -inf mask of the problem statement):
+ *   s_ij  = scale * sum_k Q[b,h,i,k] K[b,g,j,k]   for allowed (i, j), else -inf
+ *   O[b,h,i,:] = sum_j softmax_j(s_i.) V[b,g,j,:],  LSE[b,h,i] = ln sum_j exp(s_ij)
+ * with g = h / (H / H_kv) (query heads in contiguous groups share a KV head;
+ * the FlashMLA article, section 5.1, shows the one-KV-head case).
+ * Allowed keys, with off = N_kv - N_q (bottom-right alignment):
+ *   causal = 0, window <= 0 : every key j in [0, N_kv)
+ *   causal = 1              : j <= i + off
+ *   causal = 1, window > 0  : i + off - window + 1 <= j <= i + off
+ * A row with no allowed key gets O = 0 and LSE = -inf.
+ *
+ * Arguments
+ *   Q    bf16 [B, H,    N_q,  d]     K, V  bf16 [B, H_kv, N_kv, d]
+ *   O    bf16 [B, H,    N_q,  d]     (written; fp32 accumulation, rounded to nearest even)
+ *   LSE  fp32 [B, H,    N_q]         (written)
+ *   d in {64, 128};  B, H, H_kv >= 1;  H % H_kv == 0;  N_q, N_kv >= 0;
+ *   scale finite and > 0 (usually 1/sqrt(d));  causal in {0, 1};
+ *   window > 0 requires causal = 1 (else GBATTN_ERR_UNSUPPORTED).
+ * O and LSE must not overlap the inputs.
+ */
+int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+             int B, int H, int H_kv, int N_q, int N_kv, int d,
+             int causal, int window, float scale, void *stream);
+
+/*
+ * mla_decode_workspace_bytes -- size of the scratch buffer mla_decode needs
+ * for the given shape on the current device (it depends on the device's SM
+ * count).  Returns 0 for an invalid shape.
+ */
+size_t mla_decode_workspace_bytes(int B, int H, int N_kv, int d_c);
+
+/*
+ * mla_decode -- MLA decode attention, one query token per sequence.
+ *
+ * Operation (the devpress.csdn.net FlashMLA article, section 2.2: the score is
+ * the latent product plus the RoPE product accumulated into one score tile;
+ * the values are the latent rows):
+ *   s_j = scale * (Q_nope[b,h,:] . KV_latent[b,j,:] + Q_pe[b,h,:] . K_pe[b,j,:])
+ *   O[b,h,:] = sum_j softmax_j(s) KV_latent[b,j,:],   LSE[b,h] = ln sum_j exp(s_j)
+ *
+ * Arguments
+ *   Q_nope bf16 [B, H, d_c]   Q_pe bf16 [B, H, d_r]
+ *   KV_latent bf16 [B, N_kv, d_c]   K_pe bf16 [B, N_kv, d_r]
+ *   O bf16 [B, H, d_c] (written)    LSE fp32 [B, H] (written)
+ *   d_c = 512, d_r = 64, H = 128 (one 128-row tile of heads), B >= 1,
+ *   N_kv >= 1 (same for every sequence), scale finite and > 0.
+ *   workspace: device buffer of at least mla_decode_workspace_bytes(B, H,
+ *   N_kv, d_c) bytes, 16-byte aligned, owned by the caller; it holds the
+ *   per-split partial results and is overwritten.  Calls that share a
+ *   workspace must not overlap in time.
+ */
+int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+               void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gbattn_check -- synchronise `stream`, then read and clear the device status
+ * word of the current device.  Returns GBATTN_OK, GBATTN_ERR_TIMEOUT if a
+ * kernel's bounded wait ran out since the last check, or GBATTN_ERR_LAUNCH if
+ * the stream reports a CUDA error.
+ */
+int gbattn_check(void *stream);
+
+/* gbattn_last_error -- message for the calling thread's last non-OK return
+ * (empty string if none).  The pointer stays valid until the thread's next call. */
+const char *gbattn_last_error(void);
+
+/*
+ * gbattn_set_wait_timeout_ns -- limit for every device-side wait of later
+ * launches (default 2 s; clamped to [1 ms, 60 s]).  Returns the previous value.
+ */
+uint64_t gbattn_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * gbattn_selftest_umma -- layout check of the tensor-core building blocks the
+ * kernels are made of, on one 128x128x128 bf16 tile:
+ *   S = A B^T   (A, B: TMA-loaded, 128-byte-swizzled, K-major shared-memory operands)
+ *   O = P V     (P written to tensor memory from registers; V a TMA-loaded,
+ *                128-byte-swizzled, N-major shared-memory operand)
+ * A, B, P, V: bf16 [128, 128] row-major device buffers;  S, O: fp32 [128, 128].
+ * Not part of the attention computation; used by the test suite.
+ */
+int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void *V,
+                         float *S, float *O, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads, exports every declared entry point, and
+rejects bad arguments before touching the GPU (so these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests._util import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_lib()
+    import tiled_attention_flashattention_gb300 as g
+    assert os.path.samefile(path, g.library_path())
+    return g.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "mla_decode", "mla_decode_workspace_bytes", "gbattn_check",
+              "gbattn_last_error", "gbattn_set_wait_timeout_ns", "gbattn_selftest_umma"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libgbattn.so does not export {n}"
+
+
+def _attn(lib, Q=16, K=16, V=16, O=16, LSE=16, B=1, H=2, H_kv=2, N_q=8, N_kv=8, d=64, causal=0,
+          window=0, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(vp(Q), vp(K), vp(V), vp(O), vp(LSE), B, H, H_kv, N_q, N_kv, d, causal, window,
+                        ctypes.c_float(scale), None)
+
+
+def test_attn_fwd_argument_errors(lib):
+    assert _attn(lib, H=3, H_kv=2) == 1                     # H % H_kv
+    assert _attn(lib, B=-1) == 1
+    assert _attn(lib, causal=2) == 1
+    assert _attn(lib, scale=0.0) == 1
+    assert _attn(lib, scale=float("nan")) == 1
+    assert _attn(lib, d=96) == 2                            # unsupported head dim
+    assert _attn(lib, window=4, causal=0) == 2              # window needs causal
+    assert _attn(lib, Q=0) == 1                             # null pointer
+    assert _attn(lib, K=24) == 3                            # misaligned
+    assert _attn(lib, LSE=18) == 3
+    assert b"16-byte" in lib.gbattn_last_error() or b"aligned" in lib.gbattn_last_error()
+
+
+def test_mla_decode_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def mla(H=128, d_c=512, d_r=64, N_kv=64, scale=0.04, Qn=16, ws=16, wsb=1 << 20):
+        return lib.mla_decode(vp(Qn), vp(16), vp(16), vp(16), vp(16), vp(16), 2, H, N_kv, d_c, d_r,
+                              ctypes.c_float(scale), vp(ws), wsb, None)
+    assert mla(N_kv=0) == 1
+    assert mla(scale=-1.0) == 1
+    assert mla(H=64) == 2
+    assert mla(d_c=256) == 2
+    assert mla(Qn=0) == 1
+    assert mla(Qn=40) == 3

@@ -1,1 +1,187 @@
-"""GB300-native fused attention forward: tiled FlashAttention prefill and MLA decode."""
+"""GB300-native fused attention forward: tiled FlashAttention prefill and MLA decode.
+
+A thin ctypes binding over ``libgbattn.so`` (C ABI in ``include/gbattn.h``).
+The functions here only marshal arguments: they check tensor properties,
+allocate outputs with torch when the caller gives none, and pass raw device
+pointers and the current CUDA stream to the library.  Every arithmetic step
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = ["attn_fwd", "mla_decode", "mla_decode_workspace_bytes", "check", "selftest_umma",
+           "set_wait_timeout_ns", "GbattnError", "library_path", "load_library"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+_lib = None
+_lock = threading.Lock()
+
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "WORKSPACE", 5: "LAUNCH",
+           6: "TIMEOUT", 7: "ARCH"}
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"gbattn {_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libgbattn.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F, SZ, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
+        lib.attn_fwd.restype = I
+        lib.mla_decode_workspace_bytes.argtypes = [I, I, I, I]
+        lib.mla_decode_workspace_bytes.restype = SZ
+        lib.mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
+        lib.mla_decode.restype = I
+        lib.gbattn_check.argtypes = [P]
+        lib.gbattn_check.restype = I
+        lib.gbattn_last_error.argtypes = []
+        lib.gbattn_last_error.restype = ctypes.c_char_p
+        lib.gbattn_set_wait_timeout_ns.argtypes = [U64]
+        lib.gbattn_set_wait_timeout_ns.restype = U64
+        lib.gbattn_selftest_umma.argtypes = [P, P, P, P, P, P, P]
+        lib.gbattn_selftest_umma.restype = I
+        _lib = lib
+        return lib
+
+
+def _raise_if(rc: int):
+    if rc != 0:
+        msg = load_library().gbattn_last_error().decode(errors="replace")
+        raise GbattnError(rc, msg)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def attn_fwd(Q, K, V, causal: bool = False, window: int = 0, scale: float | None = None,
+             O=None, LSE=None, stream=None):
+    """Fused attention forward.  Q [B,H,N_q,d], K/V [B,H_kv,N_kv,d] bf16 CUDA tensors.
+
+    Returns (O [B,H,N_q,d] bf16, LSE [B,H,N_q] fp32).  ``window > 0`` (causal
+    only) keeps keys j in [i + N_kv - N_q - window + 1, i + N_kv - N_q].
+    Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    lib = load_library()
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q, K, V must be 4-D [B, H, N, d]")
+    B, H, N_q, d = Q.shape
+    _, H_kv, N_kv, _ = K.shape
+    _need(Q, "Q", torch.bfloat16, None)
+    _need(K, "K", torch.bfloat16, (B, H_kv, N_kv, d))
+    _need(V, "V", torch.bfloat16, (B, H_kv, N_kv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty((B, H, N_q, d), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None:
+        LSE = torch.empty((B, H, N_q), dtype=torch.float32, device=Q.device)
+    _need(O, "O", torch.bfloat16, (B, H, N_q, d))
+    _need(LSE, "LSE", torch.float32, (B, H, N_q))
+    rc = lib.attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, H_kv, N_q, N_kv, d,
+                      int(bool(causal)), int(window), float(scale), ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def mla_decode_workspace_bytes(B: int, H: int, N_kv: int, d_c: int = 512) -> int:
+    return int(load_library().mla_decode_workspace_bytes(B, H, N_kv, d_c))
+
+
+def mla_decode(Q_nope, Q_pe, KV_latent, K_pe, scale: float | None = None, O=None, LSE=None,
+               workspace=None, stream=None):
+    """MLA decode.  Q_nope [B,H,d_c], Q_pe [B,H,d_r], KV_latent [B,N_kv,d_c], K_pe [B,N_kv,d_r] bf16.
+
+    Returns (O [B,H,d_c] bf16, LSE [B,H] fp32).  ``workspace`` (a uint8 CUDA
+    tensor of at least ``mla_decode_workspace_bytes`` bytes) is allocated when
+    not given.
+    """
+    lib = load_library()
+    B, H, d_c = Q_nope.shape
+    d_r = Q_pe.shape[-1]
+    N_kv = KV_latent.shape[1]
+    _need(Q_nope, "Q_nope", torch.bfloat16, None)
+    _need(Q_pe, "Q_pe", torch.bfloat16, (B, H, d_r))
+    _need(KV_latent, "KV_latent", torch.bfloat16, (B, N_kv, d_c))
+    _need(K_pe, "K_pe", torch.bfloat16, (B, N_kv, d_r))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_c + d_r)
+    if O is None:
+        O = torch.empty((B, H, d_c), dtype=torch.bfloat16, device=Q_nope.device)
+    if LSE is None:
+        LSE = torch.empty((B, H), dtype=torch.float32, device=Q_nope.device)
+    _need(O, "O", torch.bfloat16, (B, H, d_c))
+    _need(LSE, "LSE", torch.float32, (B, H))
+    need = int(lib.mla_decode_workspace_bytes(B, H, N_kv, d_c))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=Q_nope.device)
+    _need(workspace, "workspace", torch.uint8, None)
+    rc = lib.mla_decode(_ptr(Q_nope), _ptr(Q_pe), _ptr(KV_latent), _ptr(K_pe), _ptr(O), _ptr(LSE),
+                        B, H, N_kv, d_c, d_r, float(scale), _ptr(workspace), workspace.numel(),
+                        ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def check(stream=None):
+    """Synchronise the stream and raise GbattnError if a kernel's bounded wait ran out."""
+    _raise_if(load_library().gbattn_check(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return int(load_library().gbattn_set_wait_timeout_ns(int(ns)))
+
+
+def selftest_umma(A, B, P, V, stream=None):
+    """One-tile tensor-core layout check: returns (S = A B^T, O = P V) in fp32."""
+    lib = load_library()
+    for name, t in (("A", A), ("B", B), ("P", P), ("V", V)):
+        _need(t, name, torch.bfloat16, (128, 128))
+    S = torch.empty((128, 128), dtype=torch.float32, device=A.device)
+    O = torch.empty((128, 128), dtype=torch.float32, device=A.device)
+    rc = lib.gbattn_selftest_umma(_ptr(A), _ptr(B), _ptr(P), _ptr(V), _ptr(S), _ptr(O),
+                                  ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return S, O

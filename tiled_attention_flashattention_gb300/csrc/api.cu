@@ -1,0 +1,243 @@
+// api.cu -- the C ABI of libgbattn.so (declared in include/gbattn.h):
+// argument validation, per-device state (architecture check, SM count, device
+// status word), TMA descriptor encoding, and dispatch to the kernel launchers.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "gbattn.h"
+#include "kernels.h"
+
+namespace gbattn {
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+// Device status word: kernels record the first failed bounded wait here.
+__device__ int g_status_word;
+
+struct DevInfo {
+    bool init = false;
+    int major = 0, minor = 0, num_sms = 0;
+    int *status = nullptr;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int fail(int code, const std::string &msg)
+{
+    g_err = msg;
+    return code;
+}
+
+int get_env(LaunchEnv &env, void *stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(GBATTN_ERR_LAUNCH, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.init) {
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail(GBATTN_ERR_LAUNCH, std::string("device query: ") + cudaGetErrorString(e));
+        if (d.major == 10 && d.minor == 3) {
+            if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word)) != cudaSuccess)
+                return fail(GBATTN_ERR_LAUNCH, std::string("status word: ") + cudaGetErrorString(e));
+        }
+        d.init = true;
+    }
+    if (!(d.major == 10 && d.minor == 3)) {
+        char buf[96];
+        snprintf(buf, sizeof buf, "device is sm_%d%d; this library is built for sm_103a only", d.major, d.minor);
+        return fail(GBATTN_ERR_ARCH, buf);
+    }
+    env.stream = static_cast<cudaStream_t>(stream);
+    env.status = d.status;
+    env.timeout_ns = g_timeout_ns.load();
+    env.num_sms = d.num_sms;
+    return GBATTN_OK;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool valid_scale(float s)
+{
+    return std::isfinite(s) && s > 0.f;
+}
+
+}  // namespace
+
+bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
+                      uint64_t outer, uint32_t box_rows, std::string &err)
+{
+    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static EncodeFn encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<EncodeFn>(fn);
+    });
+    if (!encode) {
+        err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    const cuuint64_t dims[3] = {cols, rows, outer};
+    const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = encode(&desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu,%llu,%llu] box rows %u",
+                 static_cast<int>(r), static_cast<unsigned long long>(outer),
+                 static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols), box_rows);
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                        int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
+                        void *stream)
+{
+    g_err.clear();
+    if (B < 0 || H < 1 || H_kv < 1 || N_q < 0 || N_kv < 0)
+        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: need B >= 0, H >= 1, H_kv >= 1, N_q >= 0, N_kv >= 0");
+    if (H % H_kv != 0) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: H must be a multiple of H_kv");
+    if (causal != 0 && causal != 1) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
+    if (d != 64 && d != 128) return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: d must be 64 or 128");
+    if (window > 0 && !causal)
+        return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: a sliding window requires causal = 1");
+    if (static_cast<long long>(B) * H * N_q > (1LL << 40) || static_cast<long long>(N_q) * d > (1LL << 31) ||
+        static_cast<long long>(N_kv) * d > (1LL << 31))
+        return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: problem too large");
+    const bool work = static_cast<long long>(B) * H * N_q > 0;
+    if (work && (!Q || !O || !LSE || (N_kv > 0 && (!K || !V))))
+        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: null tensor pointer");
+    if (work && (!aligned16(Q) || !aligned16(O) || (N_kv > 0 && (!aligned16(K) || !aligned16(V)))))
+        return fail(GBATTN_ERR_ALIGNMENT, "attn_fwd: Q, K, V and O must be 16-byte aligned");
+    if (work && (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return fail(GBATTN_ERR_ALIGNMENT, "attn_fwd: LSE must be 4-byte aligned");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    if (!work) return GBATTN_OK;
+    std::string err;
+    rc = launch_attn_fwd(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, causal, window, scale, env, err);
+    if (rc != GBATTN_OK) g_err = err;
+    return rc;
+}
+
+extern "C" size_t mla_decode_workspace_bytes(int B, int H, int N_kv, int d_c)
+{
+    if (B < 1 || H < 1 || N_kv < 1 || d_c < 1) return 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return mla_workspace_bytes(B, H, N_kv, d_c, sms);
+}
+
+extern "C" int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                          void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode: need B, H, N_kv, d_c >= 1 and d_r >= 0");
+    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode: scale must be finite and > 0");
+    if (d_c != 512 || d_r != 64 || H != 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode: supports d_c = 512, d_r = 64, H = 128");
+    if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode: problem too large");
+    if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode: null tensor pointer");
+    if (!aligned16(Q_nope) || !aligned16(Q_pe) || !aligned16(KV_latent) || !aligned16(K_pe) || !aligned16(O) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return fail(GBATTN_ERR_ALIGNMENT, "mla_decode: tensors must be 16-byte aligned (LSE 4-byte)");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    const size_t need = mla_workspace_bytes(B, H, N_kv, d_c, env.num_sms);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return fail(GBATTN_ERR_WORKSPACE, "mla_decode: workspace missing, smaller than "
+                                          "mla_decode_workspace_bytes() or not 16-byte aligned");
+    std::string err;
+    rc = launch_mla_decode(Q_nope, Q_pe, KV_latent, K_pe, O, LSE, B, H, N_kv, d_c, d_r, scale,
+                           workspace, workspace_bytes, env, err);
+    if (rc != GBATTN_OK) g_err = err;
+    return rc;
+}
+
+extern "C" int gbattn_check(void *stream)
+{
+    g_err.clear();
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(env.stream);
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("stream: ") + cudaGetErrorString(e));
+    int word = 0;
+    e = cudaMemcpy(&word, env.status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("status read: ") + cudaGetErrorString(e));
+    if (word != 0) {
+        cudaMemset(env.status, 0, sizeof(int));
+        cudaDeviceSynchronize();
+        return fail(GBATTN_ERR_TIMEOUT, "a device-side bounded wait ran out; results of the "
+                                        "affected launches are invalid");
+    }
+    return GBATTN_OK;
+}
+
+extern "C" const char *gbattn_last_error(void)
+{
+    return g_err.c_str();
+}
+
+extern "C" uint64_t gbattn_set_wait_timeout_ns(uint64_t ns)
+{
+    if (ns < 1000000ull) ns = 1000000ull;
+    if (ns > 60000000000ull) ns = 60000000000ull;
+    return g_timeout_ns.exchange(ns);
+}
+
+extern "C" int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
+                                    float *O, void *stream)
+{
+    g_err.clear();
+    if (!A || !B || !P || !V || !S || !O) return fail(GBATTN_ERR_INVALID_ARG, "selftest: null pointer");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(P) || !aligned16(V) || !aligned16(S) || !aligned16(O))
+        return fail(GBATTN_ERR_ALIGNMENT, "selftest: buffers must be 16-byte aligned");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    std::string err;
+    rc = launch_selftest_umma(A, B, P, V, S, O, env, err);
+    if (rc != GBATTN_OK) g_err = err;
+    return rc;
+}

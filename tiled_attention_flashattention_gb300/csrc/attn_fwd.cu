@@ -1,0 +1,511 @@
+// attn_fwd.cu -- fused attention forward (prefill), MHA/GQA, causal and causal
+// sliding window, for sm_103a.
+//
+// What is computed (TileLang 学习笔记, "FlashAttention 的实现" and its online
+// softmax formulas): for each query row, S = Q K^T over 128-key tiles, a
+// running row maximum m and running sum l, P = exp(S - m), and O accumulated
+// as O * exp(m_prev - m_new) + P V; at the end O / l.  The exponentials are
+// base 2 with scale * log2(e) folded into one multiply-add, as in the FlashMLA
+// article's section 3.1 (exp2(acc * scale - max * scale)).
+//
+// How it maps to the GB300 SM (one CTA per SM, 384 threads, 12 warps):
+//   warp 0       TMA producer: two Q tiles (2 x 128 rows) once, then K_j and
+//                V_j tiles into a ring of shared-memory slots (128-byte swizzle);
+//   warp 1       tensor-core issuer: S_t = Q_t K_j^T into TMEM, then
+//                O_t += P_t V_j with P_t read from TMEM (it overwrites S_t);
+//   warps 4-7    softmax of Q tile 0 (one thread per row, TMEM lane = row);
+//   warps 8-11   softmax of Q tile 1;
+//   warps 2-3    idle.
+// The two Q tiles ping-pong: while the softmax warps work on tile 0's scores,
+// the tensor core computes tile 1's scores and PV products, and vice versa
+// (FlashAttention-2's point about keeping non-matmul work off the critical
+// path, TileLang 学习笔记 "FlashAttention-2 的改进").
+//
+// TMEM (512 columns x 128 lanes of 32 bit): S0 [0,128), S1 [128,256),
+// O0 [256, 256+D), O1 [256+D, 256+2D).  P_t (bf16 pairs) overwrites the first
+// 64 columns of S_t.
+//
+// The running maximum is updated lazily: the reference maximum m_ref moves
+// only when a new score exceeds it by more than 8 in log2 units.  Until then
+// the exponentials use the stale m_ref (values up to 2^8), which is exact in
+// the end because O and l are divided by the same l built with the same
+// m_ref; it avoids rescaling O (a TMEM round trip) on almost every tile.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int kBM = 128;       // query rows per Q tile
+constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kQTiles = 2;     // Q tiles per CTA
+constexpr int kThreads = 384;
+constexpr int kChunkBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
+constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (log2 units)
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = kBM * D * 2;
+    static constexpr int kSlots = (D == 128) ? 5 : 10;
+    static constexpr uint32_t kTmemCols = 512;
+    // TMEM columns of S_t (P_t overwrites its first 64) and O_t.
+    __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+    __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + D * t; }
+};
+
+struct Ctl {
+    uint64_t q_full;
+    uint64_t full[10];
+    uint64_t empty[10];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_final[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+constexpr size_t smem_bytes()
+{
+    return 1024 + static_cast<size_t>(kQTiles + Cfg<D>::kSlots) * Cfg<D>::kTileBytes + sizeof(Ctl);
+}
+
+struct Params {
+    __nv_bfloat16 *O;
+    float *LSE;
+    int B, H, H_kv, N_q, N_kv;
+    int causal, window;
+    int group;          // H / H_kv
+    int n_qblk;         // ceil(N_q / 256)
+    float c;            // scale * log2(e)
+    int *status;
+    uint64_t timeout_ns;
+};
+
+struct Range {
+    int lo, hi;         // KV tiles [lo, hi); empty when lo >= hi
+};
+
+// KV tiles touched by query rows [r0, r1) (r1 > r0).
+__device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
+{
+    const int off = p.N_kv - p.N_q;
+    const int key_hi = p.causal ? min(p.N_kv, r1 + off) : p.N_kv;          // exclusive
+    const int key_lo = p.window > 0 ? max(0, r0 + off - p.window + 1) : 0;  // inclusive
+    if (key_hi <= key_lo) return {0, 0};
+    return {key_lo / kBN, (key_hi + kBN - 1) / kBN};
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;                                    // [2][TileBytes]
+    uint8_t *ring = smem + kQTiles * C::kTileBytes;        // [Slots][TileBytes]
+    Ctl &c = *reinterpret_cast<Ctl *>(ring + C::kSlots * C::kTileBytes);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    // ---- work item: (batch, head, 256-row query block), longest first
+    const int nbh = p.B * p.H;
+    const int bh = blockIdx.x % nbh;
+    const int qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / nbh);
+    const int b = bh / p.H, h = bh % p.H;
+    const int kvh = b * p.H_kv + h / p.group;
+    int r0[2], r1[2];
+    Range rng[2];
+    bool has[2];
+    int lo = 0x7fffffff, hi = -1;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        r0[t] = qb * (kQTiles * kBM) + t * kBM;
+        r1[t] = min(r0[t] + kBM, p.N_q);
+        rng[t] = (r0[t] < p.N_q) ? kv_range(r0[t], r1[t], p) : Range{0, 0};
+        has[t] = rng[t].lo < rng[t].hi;
+        if (has[t]) {
+            lo = min(lo, rng[t].lo);
+            hi = max(hi, rng[t].hi);
+        }
+    }
+    if (lo > hi) lo = hi = 0;
+
+    // ---- setup
+    if (threadIdx.x == 0) {
+        mbar_init(&c.q_full, 1);
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(&c.full[i], 1);
+            mbar_init(&c.empty[i], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&c.s_full[t], 1);
+            mbar_init(&c.p_full[t], 4 * 32);
+            mbar_init(&c.o_final[t], 1);
+        }
+        mbar_init(&c.drain, 1);
+        c.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, C::kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tbase = c.tmem_base;
+    const WaitCtl ctl{&c.abort, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t qbytes = 0;
+            for (int t = 0; t < 2; ++t)
+                if (has[t]) qbytes += C::kTileBytes;
+            if (qbytes) {
+                mbar_arrive_expect_tx(&c.q_full, qbytes);
+                for (int t = 0; t < 2; ++t)
+                    if (has[t])
+                        for (int ch = 0; ch < C::kChunks; ++ch)
+                            tma_load_3d(sQ + t * C::kTileBytes + ch * kChunkBytes, &tmQ, &c.q_full,
+                                        ch * 64, r0[t], bh);
+            }
+            bool ok = true;
+            int it = 0;
+            for (int j = lo; j < hi && ok; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int slot = it % C::kSlots;
+                    const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
+                    if (round > 0 && !(ok = mbar_wait(&c.empty[slot], (round & 1u) ^ 1u, ctl))) break;
+                    mbar_arrive_expect_tx(&c.full[slot], C::kTileBytes);
+                    const CUtensorMap *m = kv ? &tmV : &tmK;
+                    for (int ch = 0; ch < C::kChunks; ++ch)
+                        tma_load_3d(ring + slot * C::kTileBytes + ch * kChunkBytes, m, &c.full[slot],
+                                    ch * 64, j * kBN, kvh);
+                    ++it;
+                }
+            }
+            if (!ok) {
+                // Aborted: let every load already issued land before the CTA exits.
+                volatile int no_abort = 0;
+                const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+                if (qbytes) mbar_wait(&c.q_full, 0, drain);
+                for (int i = (it > C::kSlots ? it - C::kSlots : 0); i < it; ++i)
+                    mbar_wait(&c.full[i % C::kSlots], static_cast<uint32_t>(i / C::kSlots) & 1u, drain);
+            }
+        }
+    } else if (warp == 1) {
+        // =================== tensor-core issuer ===================
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
+            const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
+            // S_t = Q_t K^T: K-major A and B, 16 bf16 (32 B) per MMA along d.
+            auto issue_S = [&](int t, int slot) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t koff = (k / 4) * kChunkBytes + (k % 4) * 32;
+                    const uint64_t a = smem_desc_sw128(sQa + t * C::kTileBytes + koff, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes + koff, 16, 1024);
+                    umma_ss(tbase + C::col_s(t), a, bd, idS, k > 0 ? 1u : 0u);
+                }
+            };
+            // O_t += P_t V: P from TMEM (8 columns per 16 keys), V N-major
+            // (64-wide d chunks 16 KB apart, 16 keys = 2048 B per MMA).
+            bool started[2] = {false, false};
+            auto issue_PV = [&](int t, int slot) {
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint64_t bd =
+                        smem_desc_sw128(ringa + slot * C::kTileBytes + k * 2048, kChunkBytes, 1024);
+                    umma_ts(tbase + C::col_o(t), tbase + C::col_s(t) + k * 8, bd, idPV,
+                            (started[t] || k > 0) ? 1u : 0u);
+                }
+                started[t] = true;
+            };
+            auto in_rng = [&](int t, int j) { return j >= rng[t].lo && j < rng[t].hi; };
+
+            bool ok = true;
+            if (hi > lo) ok = mbar_wait(&c.q_full, 0, ctl);
+            int it = 0;
+            uint32_t pcount[2] = {0, 0};
+            if (ok && hi > lo) {
+                const int slotK = 0;
+                ok = mbar_wait(&c.full[slotK], 0, ctl);
+                ++it;
+                if (ok) {
+                    tc_fence_after_sync();
+                    for (int t = 0; t < 2; ++t)
+                        if (in_rng(t, lo)) {
+                            issue_S(t, slotK);
+                            umma_commit(&c.s_full[t]);
+                        }
+                    umma_commit(&c.empty[slotK]);
+                }
+            }
+            for (int j = lo; j < hi && ok; ++j) {
+                const int slotV = it % C::kSlots;
+                if (!(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
+                    break;
+                ++it;
+                if (in_rng(0, j)) {
+                    if (!(ok = mbar_wait(&c.p_full[0], pcount[0]++ & 1u, ctl))) break;
+                    tc_fence_after_sync();
+                    issue_PV(0, slotV);
+                }
+                int slotK = -1;
+                if (j + 1 < hi) {
+                    slotK = it % C::kSlots;
+                    if (!(ok = mbar_wait(&c.full[slotK], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
+                        break;
+                    ++it;
+                    if (in_rng(0, j + 1)) {
+                        issue_S(0, slotK);
+                        umma_commit(&c.s_full[0]);
+                    }
+                }
+                if (in_rng(1, j)) {
+                    if (!(ok = mbar_wait(&c.p_full[1], pcount[1]++ & 1u, ctl))) break;
+                    tc_fence_after_sync();
+                    issue_PV(1, slotV);
+                }
+                umma_commit(&c.empty[slotV]);
+                if (slotK >= 0) {
+                    if (in_rng(1, j + 1)) {
+                        issue_S(1, slotK);
+                        umma_commit(&c.s_full[1]);
+                    }
+                    umma_commit(&c.empty[slotK]);
+                }
+            }
+            for (int t = 0; t < 2; ++t)
+                if (has[t]) umma_commit(&c.o_final[t]);
+            // No tensor-core work may still be in flight when TMEM is freed.
+            umma_commit(&c.drain);
+            volatile int no_abort = 0;
+            const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+            mbar_wait(&c.drain, 0, drain);
+        }
+    } else if (warp >= 4) {
+        // =================== softmax: one thread per query row ===================
+        const int t = (warp - 4) / 4;
+        const int quad = warp % 4;                 // TMEM lanes [32*quad, 32*quad+32)
+        const int row = r0[t] + quad * 32 + lane;
+        const bool row_valid = row < p.N_q && r0[t] < p.N_q;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tbase + lane_base + C::col_s(t);
+        const uint32_t tO = tbase + lane_base + C::col_o(t);
+        const float cexp = p.c;
+        const float thr = kRescaleLog2 / cexp;     // threshold in raw score units
+        const int off = p.N_kv - p.N_q;
+        const int key_max = row + off;             // causal: keys <= key_max
+        const int key_min = row + off - p.window + 1;
+
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        int n = 0;
+        for (int j = rng[t].lo; j < rng[t].hi && ok; ++j, ++n) {
+            // tcgen05.ld/st below are warp-collective: keep the outcome warp-uniform.
+            ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[t], static_cast<uint32_t>(n) & 1u, ctl));
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t sr[128];
+            tmem_ld_x128(tS, sr);
+            float s[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+
+            const int k0 = j * kBN;
+            const bool need_mask = (k0 + kBN > p.N_kv) ||
+                                   (p.causal && k0 + kBN - 1 > r0[t] + off) ||
+                                   (p.window > 0 && k0 < (r1[t] - 1) + off - p.window + 1);
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int key = k0 + i;
+                    const bool allowed = key < p.N_kv && (!p.causal || key <= key_max) &&
+                                         (p.window <= 0 || key >= key_min);
+                    if (!allowed) s[i] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+
+            const bool move = mx > m_ref + thr;
+            const float new_ref = move ? mx : m_ref;
+            const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
+            l *= alpha;
+            if (n > 0 && __any_sync(0xffffffffu, move)) {
+                // O_t already holds the PV products of earlier tiles (their
+                // completion is covered by this tile's S commit): rescale it.
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + ch * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_x32(tO + ch * 32, o);
+                }
+            }
+            m_ref = new_ref;
+            const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[q * 32 + 2 * i], cexp, -base));
+                    const float p1 = ex2_approx(fmaf(s[q * 32 + 2 * i + 1], cexp, -base));
+                    sum += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_x16(tS + q * 16, pk);
+            }
+            l += sum;
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&c.p_full[t]);
+        }
+
+        // ---- epilogue: O / l -> bf16, LSE
+        const size_t out_row = (static_cast<size_t>(b) * p.H + h) * p.N_q + row;
+        if (has[t] && ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&c.o_final[t], 0, ctl));
+            if (ok) {
+                tc_fence_after_sync();
+                const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + ch * 32, o);
+                    uint4 v[4];
+                    uint32_t *w = reinterpret_cast<uint32_t *>(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                           __uint_as_float(o[2 * i + 1]) * inv_l);
+                    if (row_valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.O + out_row * D + ch * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                    }
+                }
+                if (row_valid)
+                    p.LSE[out_row] = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (!has[t] && row_valid) {
+            // No key is visible to any row of this tile.
+            uint4 *dst = reinterpret_cast<uint4 *>(p.O + out_row * D);
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+            p.LSE[out_row] = -INFINITY;
+        }
+    }
+
+    // ---- teardown (lanes 1-31 of warps 0 and 1 wait here for their lane 0)
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, C::kTmemCols);
+    }
+}
+
+template <int D>
+int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
+           int grid, const LaunchEnv &env, std::string &err)
+{
+    static bool configured = false;   // per process; attribute is per function
+    const size_t smem = smem_bytes<D>();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+            return 5;
+        }
+        configured = true;
+    }
+    attn_fwd_kernel<D><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
+        return 5;
+    }
+    return 0;
+}
+
+// Writes O = 0, LSE = -inf for every row (used when N_kv == 0).
+__global__ void fill_empty_kernel(__nv_bfloat16 *O, float *LSE, size_t rows, int d)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < rows;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        for (int k = 0; k < d; ++k) O[i * d + k] = __float2bfloat16(0.f);
+        LSE[i] = -INFINITY;
+    }
+}
+
+}  // namespace
+
+int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                    int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
+                    const LaunchEnv &env, std::string &err)
+{
+    if (N_q == 0 || B == 0) return 0;
+    if (N_kv == 0) {
+        const size_t rows = static_cast<size_t>(B) * H * N_q;
+        fill_empty_kernel<<<static_cast<int>(std::min<size_t>((rows + 255) / 256, 4096)), 256, 0,
+                            env.stream>>>(static_cast<__nv_bfloat16 *>(O), LSE, rows, d);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            err = std::string("fill launch: ") + cudaGetErrorString(e);
+            return 5;
+        }
+        return 0;
+    }
+    CUtensorMap tq, tk, tv;
+    if (!make_tma_bf16_3d(tq, Q, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
+        !make_tma_bf16_3d(tk, K, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err) ||
+        !make_tma_bf16_3d(tv, V, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err))
+        return 5;
+    Params p;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.B = B;
+    p.H = H;
+    p.H_kv = H_kv;
+    p.N_q = N_q;
+    p.N_kv = N_kv;
+    p.causal = causal;
+    p.window = window > 0 ? window : 0;
+    p.group = H / H_kv;
+    p.n_qblk = (N_q + kQTiles * kBM - 1) / (kQTiles * kBM);
+    p.c = scale * 1.4426950408889634f;
+    p.status = env.status;
+    p.timeout_ns = env.timeout_ns;
+    const long long grid = static_cast<long long>(p.n_qblk) * B * H;
+    if (grid > 0x7fffffffLL) {
+        err = "attn_fwd: problem too large for one launch";
+        return 2;
+    }
+    if (d == 128) return launch<128>(tq, tk, tv, p, static_cast<int>(grid), env, err);
+    return launch<64>(tq, tk, tv, p, static_cast<int>(grid), env, err);
+}
+
+}  // namespace gbattn

@@ -1,0 +1,45 @@
+// kernels.h -- host-side declarations shared by the C-ABI layer and the
+// kernel translation units of libgbattn.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gbattn {
+
+struct LaunchEnv {
+    cudaStream_t stream;
+    int *status;          // device status word of the current device
+    uint64_t timeout_ns;  // limit of every device-side wait
+    int num_sms;          // SM count of the current device
+};
+
+// Prefill attention forward (attn_fwd).  Pointers are device pointers, already
+// validated by the caller; returns a gbattn_status value.
+int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                    int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
+                    const LaunchEnv &env, std::string &err);
+
+// MLA decode (mla_decode).
+size_t mla_workspace_bytes(int B, int H, int N_kv, int d_c, int num_sms);
+int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                      void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                      void *workspace, size_t workspace_bytes, const LaunchEnv &env,
+                      std::string &err);
+
+// Tensor-core layout self test (gbattn_selftest_umma).
+int launch_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
+                         float *O, const LaunchEnv &env, std::string &err);
+
+// Build a 128-byte-swizzled bf16 TMA descriptor for a row-major tensor viewed
+// as [outer][rows][cols] (cols contiguous, cols % 8 == 0), with a box of 64
+// columns x box_rows rows x 1.  Out-of-range box elements read as zero.
+// Returns false and fills err on failure.
+bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
+                      uint64_t outer, uint32_t box_rows, std::string &err);
+
+}  // namespace gbattn
