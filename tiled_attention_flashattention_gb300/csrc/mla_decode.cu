@@ -1,16 +1,544 @@
-// mla_decode.cu -- placeholder until the MLA decode kernels land.
+// mla_decode.cu -- MLA decode attention for sm_103a: one query token per
+// sequence, 128 query heads sharing one latent KV head (512 dims) plus a
+// 64-dim RoPE key part; the values are the latent rows.
+//
+// What is computed (the devpress.csdn.net FlashMLA article, section 2.2): per
+// key tile, the score tile is the latent product Q_nope KV^T plus the RoPE
+// product Q_pe K_pe^T accumulated into one accumulator, followed by the
+// exp2-based running max / running sum update of its section 3.1 and the
+// value product P KV.  The heads form the rows of the tile (section 3.2: the
+// query tile is [heads, dim]).
+//
+// GB300 mapping.  The fp32 output accumulator of 128 heads x 512 latent dims
+// fills one SM's whole tensor memory, so a pair of CTAs (a 2-CTA cluster)
+// shares each work item and splits both the contraction and the output:
+//   CTA 0 holds latent dims [0, 256): its Q and KV tiles cover those dims, it
+//         computes the partial score over them and owns O[:, 0:256);
+//   CTA 1 holds latent dims [256, 512) plus the 64 RoPE dims, computes the
+//         partial score over those 320 dims and owns O[:, 256:512).
+// Every KV byte is read from HBM by exactly one CTA.  The two fp32 partial
+// score tiles (128 heads x 64 keys) are swapped through distributed shared
+// memory, so both CTAs hold the same full score tile and run the same online
+// softmax; each then multiplies P by its own latent half (V = KV_latent).
+//
+// Work split: the B * ceil(N_kv / 64) key tiles are cut into one contiguous
+// range per cluster (as many clusters as fit on the GPU at once).  A range
+// that covers a whole sequence writes the final O and LSE; a partial range
+// writes O / l and its LSE to the workspace, and a small combine kernel merges
+// the pieces of each split sequence with the exact log-sum-exp rule
+// (TileLang 学习笔记, "Online Softmax 的关键", applied across key ranges).
+//
+// Per CTA (256 threads): warp 0 issues TMA loads, warp 1 issues tcgen05 MMAs,
+// warps 4-7 (one thread per head) exchange partial scores, run the softmax and
+// the epilogue.  TMEM: O half [0, 256), score tiles S0 [256, 320) and
+// S1 [320, 384) (double-buffered; P overwrites the first 32 columns).
+#include <cmath>
+
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace gbattn {
+namespace {
 
-size_t mla_workspace_bytes(int, int, int, int, int) { return 0; }
+constexpr int kH = 128;                   // heads per tile (MMA M)
+constexpr int kBN = 64;                   // keys per tile
+constexpr int kDc = 512;
+constexpr int kHalf = 256;                // latent dims owned by one CTA
+constexpr int kQChunk = 128 * 128;        // [128 heads x 64 dims] bf16
+constexpr int kKvChunk = kBN * 128;       // [64 keys x 64 dims] bf16
+constexpr int kMaxChunks = 5;
+constexpr int kStages = 2;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS = 256;           // S[buf] at kColS + 64 * buf
+constexpr int kXBytes = kH * kBN * 4;     // one partial-score exchange buffer
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
 
-int launch_mla_decode(const void *, const void *, const void *, const void *, void *, float *, int,
-                      int, int, int, int, float, void *, size_t, const LaunchEnv &,
-                      std::string &err)
+struct Ctl {
+    uint64_t q_full, q_empty;
+    uint64_t full[kStages], empty[kStages];
+    uint64_t s_full[2], p_full[2];
+    uint64_t pv_done;
+    uint64_t o_empty;
+    uint64_t xfull[2], xfree[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kMaxChunks) * kQChunk + static_cast<size_t>(kStages) * kMaxChunks * kKvChunk +
+    2 * static_cast<size_t>(kXBytes) + sizeof(Ctl);
+
+struct Params {
+    __nv_bfloat16 *O;
+    float *LSE;
+    float *ws_O;        // [slots][128][512] fp32, O / l of partial ranges
+    float *ws_LSE;      // [slots][128]
+    int B, N_kv, ntile;
+    long long T;        // B * ntile
+    int C;              // clusters
+    int max_seg;        // workspace slots per cluster
+    float c;            // scale * log2(e)
+    int *status;
+    uint64_t timeout_ns;
+};
+
+// Key-tile range of cluster cl: [range_start(cl), range_start(cl + 1)).
+__host__ __device__ __forceinline__ long long range_start(long long cl, long long T, int C)
 {
-    err = "mla_decode: not built yet";
-    return 2;
+    return cl * T / C;
+}
+
+// The cluster whose range holds flat tile x.
+__host__ __device__ __forceinline__ int cluster_of_tile(long long x, long long T, int C)
+{
+    return static_cast<int>(((x + 1) * C - 1) / T);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_split_kernel(const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp,
+                     const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
+                     const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sKV = sQ + kMaxChunks * kQChunk;                       // [stage][chunk]
+    uint8_t *sX = sKV + kStages * kMaxChunks * kKvChunk;            // [2][128][64] fp32, swizzled
+    Ctl &c = *reinterpret_cast<Ctl *>(sX + 2 * kXBytes);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+    const int cl = blockIdx.x / 2;
+    const long long t_begin = range_start(cl, p.T, p.C), t_end = range_start(cl + 1, p.T, p.C);
+    const int nch = rank == 0 ? 4 : 5;              // contraction chunks of this CTA
+    const int dim0 = static_cast<int>(rank) * kHalf;
+    const int b_first = static_cast<int>(t_begin / p.ntile);
+    const int b_last = t_end > t_begin ? static_cast<int>((t_end - 1) / p.ntile) : b_first - 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&c.q_full, 1);
+        mbar_init(&c.q_empty, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&c.full[s], 1);
+            mbar_init(&c.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&c.s_full[i], 1);
+            mbar_init(&c.p_full[i], 128);
+            mbar_init(&c.xfull[i], 128);
+            mbar_init(&c.xfree[i], 128);
+        }
+        mbar_init(&c.pv_done, 1);
+        mbar_init(&c.o_empty, 128);
+        mbar_init(&c.drain, 1);
+        c.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    cluster_sync_all();            // the peer's barriers exist before any remote arrive
+    tc_fence_after_sync();
+    const uint32_t tbase = c.tmem_base;
+    const WaitCtl ctl{&c.abort, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQn);
+            tma_prefetch_desc(&tmQp);
+            tma_prefetch_desc(&tmKV);
+            tma_prefetch_desc(&tmKp);
+            bool ok = true;
+            int it = 0, seg = 0, q_issued = 0;
+            const uint32_t qbytes = nch * kQChunk, kvbytes = nch * kKvChunk;
+            for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
+                const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
+                const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+                if (seg > 0 && !(ok = mbar_wait(&c.q_empty, (seg - 1) & 1, ctl))) break;
+                mbar_arrive_expect_tx(&c.q_full, qbytes);
+                for (int ch = 0; ch < 4; ++ch)
+                    tma_load_3d(sQ + ch * kQChunk, &tmQn, &c.q_full, dim0 + ch * 64, 0, b);
+                if (rank == 1) tma_load_3d(sQ + 4 * kQChunk, &tmQp, &c.q_full, 0, 0, b);
+                ++q_issued;
+                for (long long x = x0; x < x1; ++x) {
+                    const int key0 = static_cast<int>(x - static_cast<long long>(b) * p.ntile) * kBN;
+                    const int s = it % kStages;
+                    const uint32_t round = static_cast<uint32_t>(it / kStages);
+                    if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
+                    uint8_t *dst = sKV + s * kMaxChunks * kKvChunk;
+                    mbar_arrive_expect_tx(&c.full[s], kvbytes);
+                    for (int ch = 0; ch < 4; ++ch)
+                        tma_load_3d(dst + ch * kKvChunk, &tmKV, &c.full[s], dim0 + ch * 64, key0, b);
+                    if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, key0, b);
+                    ++it;
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+                if (q_issued > 0) mbar_wait(&c.q_full, (q_issued - 1) & 1, drain);
+                for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
+                    mbar_wait(&c.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, drain);
+            }
+        }
+    } else if (warp == 1) {
+        // =================== tensor-core issuer ===================
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kH, kBN, false, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(kH, kHalf, false, true);
+            const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+            bool ok = true;
+            int it = 0, seg = 0;
+            uint32_t g = 0;      // global tile counter (S buffer = g % 2)
+            // O += P V for tile gp held in stage sp.
+            auto issue_pv = [&](uint32_t gp, int sp, bool first) -> bool {
+                if (!mbar_wait(&c.p_full[gp & 1], (gp >> 1) & 1u, ctl)) return false;
+                if (first && seg > 0 && !mbar_wait(&c.o_empty, (seg - 1) & 1, ctl)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint64_t bd =
+                        smem_desc_sw128(sKVa + sp * kMaxChunks * kKvChunk + k * 2048, kKvChunk, 1024);
+                    umma_ts(tbase + kColO, tbase + kColS + 64 * (gp & 1) + k * 8, bd, idPV,
+                            (!first || k > 0) ? 1u : 0u);
+                }
+                umma_commit(&c.pv_done);
+                umma_commit(&c.empty[sp]);
+                return true;
+            };
+            for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
+                const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
+                const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+                const int n = static_cast<int>(x1 - x0);
+                if (!(ok = mbar_wait(&c.q_full, seg & 1, ctl))) break;
+                int prev_stage = -1;
+                for (int i = 0; i < n; ++i) {
+                    const int s = it % kStages;
+                    if (!(ok = mbar_wait(&c.full[s], static_cast<uint32_t>(it / kStages) & 1u, ctl))) break;
+                    tc_fence_after_sync();
+                    const uint32_t dS = tbase + kColS + 64 * (g & 1);
+                    for (int k = 0; k < nch * 4; ++k) {
+                        const uint32_t koff = (k / 4) * kQChunk + (k % 4) * 32;
+                        const uint32_t kvoff = s * kMaxChunks * kKvChunk + (k / 4) * kKvChunk + (k % 4) * 32;
+                        umma_ss(dS, smem_desc_sw128(sQa + koff, 16, 1024),
+                                smem_desc_sw128(sKVa + kvoff, 16, 1024), idS, k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&c.s_full[g & 1]);
+                    if (i == n - 1) umma_commit(&c.q_empty);
+                    if (i > 0 && !(ok = issue_pv(g - 1, prev_stage, i == 1))) break;
+                    prev_stage = s;
+                    ++it;
+                    ++g;
+                }
+                if (ok && n > 0) ok = issue_pv(g - 1, prev_stage, n == 1);
+            }
+            umma_commit(&c.drain);
+            volatile int no_abort = 0;
+            const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+            mbar_wait(&c.drain, 0, drain);
+        }
+    } else if (warp >= 4) {
+        // =================== exchange + softmax + epilogue (one thread per head) ===================
+        const int quad = warp - 4;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tO = tbase + lane_base + kColO;
+        const float cexp = p.c;
+        const float thr = kRescaleLog2 / cexp;
+        const uint32_t swz = static_cast<uint32_t>(row & 15);
+        const uint32_t my_x[2] = {smem_u32(sX) + row * 256, smem_u32(sX + kXBytes) + row * 256};
+        const uint32_t peer_x[2] = {mapa_shared(my_x[0], peer), mapa_shared(my_x[1], peer)};
+        const uint32_t peer_xfull[2] = {mapa_shared(smem_u32(&c.xfull[0]), peer),
+                                        mapa_shared(smem_u32(&c.xfull[1]), peer)};
+        const uint32_t peer_xfree[2] = {mapa_shared(smem_u32(&c.xfree[0]), peer),
+                                        mapa_shared(smem_u32(&c.xfree[1]), peer)};
+        bool ok = true;
+        uint32_t g = 0;
+        int seg = 0;
+        for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
+            const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
+            const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+            const int n = static_cast<int>(x1 - x0);
+            float m_ref = -INFINITY, l = 0.f;
+            for (int i = 0; i < n; ++i, ++g) {
+                const uint32_t buf = g & 1, use = g >> 1;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[buf], use & 1u, ctl)))) break;
+                tc_fence_after_sync();
+                const uint32_t tS = tbase + lane_base + kColS + 64 * buf;
+                uint32_t sr[64];
+                tmem_ld_x64(tS, sr);
+                // send this CTA's partial row to the peer, receive the peer's
+                if (use > 0 && !(ok = __all_sync(0xffffffffu,
+                                                 mbar_wait_cluster(&c.xfree[buf], (use - 1) & 1u, ctl))))
+                    break;
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    st_cluster_v4(peer_x[buf] + ((q ^ swz) << 4), __uint_as_float(sr[4 * q]),
+                                  __uint_as_float(sr[4 * q + 1]), __uint_as_float(sr[4 * q + 2]),
+                                  __uint_as_float(sr[4 * q + 3]));
+                mbar_arrive_remote(peer_xfull[buf]);
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait_cluster(&c.xfull[buf], use & 1u, ctl)))) break;
+                float s[64];
+                const float4 *xin = reinterpret_cast<const float4 *>(sX + buf * kXBytes + row * 256);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 v = xin[q ^ swz];
+                    s[4 * q] = __uint_as_float(sr[4 * q]) + v.x;
+                    s[4 * q + 1] = __uint_as_float(sr[4 * q + 1]) + v.y;
+                    s[4 * q + 2] = __uint_as_float(sr[4 * q + 2]) + v.z;
+                    s[4 * q + 3] = __uint_as_float(sr[4 * q + 3]) + v.w;
+                }
+                mbar_arrive_remote(peer_xfree[buf]);
+
+                const int key0 = static_cast<int>(x0 + i - static_cast<long long>(b) * p.ntile) * kBN;
+                if (key0 + kBN > p.N_kv) {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k)
+                        if (key0 + k >= p.N_kv) s[k] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
+                const bool move = mx > m_ref + thr;
+                const float new_ref = move ? mx : m_ref;
+                const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
+                l *= alpha;
+                if (i > 0 && __any_sync(0xffffffffu, move)) {
+                    // O holds the PV products up to the previous tile; wait for the last one.
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.pv_done, (g - 1) & 1u, ctl)))) break;
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int ch = 0; ch < kHalf / 32; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld_x32(tO + ch * 32, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st_x32(tO + ch * 32, o);
+                    }
+                }
+                m_ref = new_ref;
+                const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
+                float sum = 0.f;
+                uint32_t pk[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
+                    const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
+                    sum += p0 + p1;
+                    pk[k] = pack_bf16x2(p0, p1);
+                }
+                l += sum;
+                tmem_st_x32(tS, pk);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(&c.p_full[buf]);
+            }
+            if (!ok) break;
+
+            // ---- epilogue of this range of sequence b
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.pv_done, (g - 1) & 1u, ctl)))) break;
+            tc_fence_after_sync();
+            const bool whole = (n == p.ntile);
+            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+            const float lse = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
+            const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - b_first);
+#pragma unroll 1
+            for (int ch = 0; ch < kHalf / 32; ++ch) {
+                uint32_t o[32];
+                tmem_ld_x32(tO + ch * 32, o);
+                if (whole) {
+                    uint4 v[4];
+                    uint32_t *w = reinterpret_cast<uint32_t *>(v);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * kH + row) * kDc +
+                                                           dim0 + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_O + (slot * kH + row) * kDc + dim0 + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                             __uint_as_float(o[4 * k + 2]) * inv_l,
+                                             __uint_as_float(o[4 * k + 3]) * inv_l);
+                }
+            }
+            if (rank == 0) {
+                if (whole)
+                    p.LSE[static_cast<size_t>(b) * kH + row] = lse;
+                else
+                    p.ws_LSE[slot * kH + row] = lse;
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&c.o_empty);
+        }
+    }
+
+    // ---- teardown: no MMA or TMA in flight (drained above); the peer must be
+    // done with this CTA's shared memory before either CTA exits.
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// Merge the partial ranges of each split sequence: LSE = ln sum_s e^{LSE_s},
+// O = sum_s e^{LSE_s - LSE} O_s.  One block of 128 threads per (sequence,
+// head); sequences written whole by the split kernel are skipped.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const Params p)
+{
+    const int b = blockIdx.x / kH, h = blockIdx.x % kH;
+    const long long x0 = static_cast<long long>(b) * p.ntile;
+    const int c0 = cluster_of_tile(x0, p.T, p.C);
+    const int c1 = cluster_of_tile(x0 + p.ntile - 1, p.T, p.C);
+    if (c0 == c1) return;
+    float mx = -INFINITY;
+    for (int cl = c0; cl <= c1; ++cl) {
+        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        mx = fmaxf(mx, p.ws_LSE[slot * kH + h]);
+    }
+    float denom = 0.f;
+    for (int cl = c0; cl <= c1; ++cl) {
+        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        denom += expf(p.ws_LSE[slot * kH + h] - mx);
+    }
+    const float lse = mx + logf(denom);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cl = c0; cl <= c1; ++cl) {
+        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        const float w = expf(p.ws_LSE[slot * kH + h] - lse);
+        const float4 v = reinterpret_cast<const float4 *>(p.ws_O + (slot * kH + h) * kDc)[threadIdx.x];
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+    }
+    uint2 out;
+    out.x = pack_bf16x2(acc.x, acc.y);
+    out.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2 *>(p.O + (static_cast<size_t>(b) * kH + h) * kDc)[threadIdx.x] = out;
+    if (threadIdx.x == 0) p.LSE[static_cast<size_t>(b) * kH + h] = lse;
+}
+
+struct Plan {
+    int ntile, C, max_seg;
+    long long T;
+    size_t slots;
+};
+
+// Cluster count: as many 2-CTA clusters as are co-resident on the device
+// (queried once per process), never more than the number of key tiles.
+int resident_clusters(int num_sms)
+{
+    static int cached = -1;
+    if (cached > 0) return cached;
+    int n = 0;
+    if (cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, mla_split_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    if (n <= 0) n = num_sms / 2;
+    cached = n;
+    return n;
+}
+
+Plan make_plan(int B, int N_kv, int clusters)
+{
+    Plan pl;
+    pl.ntile = (N_kv + kBN - 1) / kBN;
+    pl.T = static_cast<long long>(B) * pl.ntile;
+    pl.C = static_cast<int>(std::min<long long>(clusters, pl.T));
+    const long long per = (pl.T + pl.C - 1) / pl.C;
+    pl.max_seg = static_cast<int>((per + pl.ntile - 1) / pl.ntile) + 1;
+    pl.slots = static_cast<size_t>(pl.C) * pl.max_seg;
+    return pl;
+}
+
+size_t plan_bytes(const Plan &pl)
+{
+    return pl.slots * kH * kDc * sizeof(float) + pl.slots * kH * sizeof(float);
+}
+
+}  // namespace
+
+size_t mla_workspace_bytes(int B, int H, int N_kv, int d_c, int num_sms)
+{
+    if (B < 1 || H != kH || N_kv < 1 || d_c != kDc) return 0;
+    return plan_bytes(make_plan(B, N_kv, resident_clusters(num_sms)));
+}
+
+int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe, void *O,
+                      float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale, void *workspace,
+                      size_t workspace_bytes, const LaunchEnv &env, std::string &err)
+{
+    const Plan pl = make_plan(B, N_kv, resident_clusters(env.num_sms));
+    if (workspace_bytes < plan_bytes(pl)) {
+        err = "mla_decode: workspace too small";
+        return 4;
+    }
+    CUtensorMap tqn, tqp, tkv, tkp;
+    if (!make_tma_bf16_3d(tqn, Q_nope, d_c, H, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, H, B, kH, err) ||
+        !make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) ||
+        !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err))
+        return 5;
+    Params p;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.ws_O = static_cast<float *>(workspace);
+    p.ws_LSE = p.ws_O + pl.slots * kH * kDc;
+    p.B = B;
+    p.N_kv = N_kv;
+    p.ntile = pl.ntile;
+    p.T = pl.T;
+    p.C = pl.C;
+    p.max_seg = pl.max_seg;
+    p.c = scale * 1.4426950408889634f;
+    p.status = env.status;
+    p.timeout_ns = env.timeout_ns;
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess) {
+        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tqn, tqp, tkv, tkp, p);
+        e = cudaGetLastError();
+    }
+    bool split = false;   // does a cluster range boundary fall inside a sequence?
+    for (int cl = 1; cl < pl.C && !split; ++cl) split = range_start(cl, pl.T, pl.C) % pl.ntile != 0;
+    if (e == cudaSuccess && split) {
+        mla_combine_kernel<<<B * kH, 128, 0, env.stream>>>(p);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        err = std::string("mla_decode launch: ") + cudaGetErrorString(e);
+        return 5;
+    }
+    return 0;
 }
 
 }  // namespace gbattn
