@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill attention forward (attn_fwd) on the MHA causal workload
+    B=4, H=16, N_q=N_kv=2048, d=128 (the headline metric, TFLOP/s), and
+  * MLA decode (mla_decode) on B=64, H=128, N_kv=4096, d_c=512, d_r=64
+    (HBM GB/s, reported in the "decode" object).
+
+Timing: W untimed warm-up steps, then K timed steps.  Inputs are resident in
+HBM; between steps a 256 MiB buffer (> the 129 MB L2) is overwritten so no
+step starts with its inputs in L2.  Each kernel call is bracketed by CUDA
+events on the launching stream (torch's current stream, which the binding
+passes to the library); the flush is outside the brackets.  The run is
+bracketed by a barrier + device synchronize on both sides and the maximum over
+ranks is taken.  FLOPs count 4*d per allowed (query, key) pair; bytes count
+each decode input read once and each output written once.
+
+--impl reference times the fp64 CPU oracle (the reference of this project)
+on a bounded sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from tiled_attention_flashattention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s and MLA-decode HBM GB/s on 1 GB300, % of roofline"
+PREFILL = "mha_causal_b4_h16_n2048_d128"
+DECODE = "mla_decode_b64_h128_nkv4096"
+FLUSH_BYTES = 256 << 20
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- workload arithmetic
+def allowed_pairs(N_q: int, N_kv: int, causal: bool, window: int) -> int:
+    """Number of (query, key) pairs the mask keeps, per (batch, head)."""
+    if not causal:
+        return N_q * N_kv
+    i = np.arange(N_q, dtype=np.int64)
+    off = N_kv - N_q
+    hi = np.minimum(N_kv - 1, i + off)
+    lo = np.maximum(0, i + off - window + 1) if window > 0 else np.zeros_like(i)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def prefill_flops(c: wl.PrefillCase) -> float:
+    return 4.0 * c.d * allowed_pairs(c.N_q, c.N_kv, c.causal, c.window) * c.B * c.H
+
+
+def prefill_bytes(c: wl.PrefillCase) -> float:
+    return 2.0 * (c.B * c.H * c.N_q * c.d * 2 + c.B * c.H_kv * c.N_kv * c.d * 2) + 4.0 * c.B * c.H * c.N_q
+
+
+def decode_flops(c: wl.MlaCase) -> float:
+    return float(c.B * c.H * c.N_kv) * (2 * (c.d_c + c.d_r) + 2 * c.d_c)
+
+
+def decode_bytes(c: wl.MlaCase) -> float:
+    kv = c.B * c.N_kv * (c.d_c + c.d_r) * 2
+    q = c.B * c.H * (c.d_c + c.d_r) * 2
+    out = c.B * c.H * c.d_c * 2 + c.B * c.H * 4
+    return float(kv + q + out)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in ("ptx.cuh",) + names:
+        with open(os.path.join(ROOT, "tiled_attention_flashattention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(kernel_key: str, source: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or
+    None when the summary is missing or the kernel source changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            d = json.load(f)[kernel_key]
+    except (OSError, KeyError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash(source) or d.get("workload") != workload:
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, flags in rows for k, v in enumerate(flags) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+def oracle_sample_rate(case, rows, kind):
+    """Time the oracle on the given rows; returns (seconds, flops)."""
+    import oracle
+    t0 = time.perf_counter()
+    if kind == "prefill":
+        Q, K, V = case["inputs"]
+        c = case["case"]
+        oracle.attn_fwd(Q, K, V, c.causal, c.window, c.softmax_scale(), rows=rows)
+        i = rows % c.N_q
+        off = c.N_kv - c.N_q
+        hi = np.minimum(c.N_kv - 1, i + off) if c.causal else np.full_like(i, c.N_kv - 1)
+        lo = np.maximum(0, i + off - c.window + 1) if c.window > 0 else np.zeros_like(i)
+        flops = float((4 * c.d * np.maximum(0, hi - lo + 1)).sum())
+    else:
+        Qn, Qp, KV, Kp = case["inputs"]
+        c = case["case"]
+        oracle.mla_decode(Qn, Qp, KV, Kp, c.softmax_scale(), rows=rows)
+        flops = float(len(rows) * c.N_kv * (2 * (c.d_c + c.d_r) + 2 * c.d_c))
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(pcase, dcase, budget_s: float):
+    """Oracle on a bounded sample: every stride-th prefill row (stride chosen
+    from a short calibration so the sample takes about budget_s)."""
+    import oracle
+    c = pcase["case"]
+    total_rows = c.B * c.H * c.N_q
+    cal_rows = np.arange(0, total_rows, max(1, total_rows // 512), dtype=np.int64)
+    dt, fl = oracle_sample_rate(pcase, cal_rows, "prefill")
+    rate = fl / max(dt, 1e-6)
+    stride = max(1, int(math.ceil(prefill_flops(c) / (rate * budget_s))))
+    rows = np.arange(0, total_rows, stride, dtype=np.int64)
+    dt, fl = oracle_sample_rate(pcase, rows, "prefill")
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle on {len(rows)} of {total_rows} query rows (every {stride}th row) of "
+                      f"{c.name}; {fl / 1e9:.1f} GFLOP in {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- main arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    pc = wl.WORKLOADS[args.workload]
+    pcase = {"case": pc, "inputs": wl.prefill_inputs(pc)}
+    import oracle
+    total_rows = pc.B * pc.H * pc.N_q
+    # size each step so that warm-up + timed steps take about 60 s of CPU time
+    cal_rows = np.arange(0, total_rows, max(1, total_rows // 256), dtype=np.int64)
+    dt, fl = oracle_sample_rate(pcase, cal_rows, "prefill")
+    rate = fl / max(dt, 1e-6)
+    per_step_s = max(0.05, 60.0 / (args.steps + args.warmup))
+    stride = max(1, int(math.ceil(prefill_flops(pc) / (rate * per_step_s))))
+    rows = np.arange(0, total_rows, stride, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_sample_rate(pcase, rows, "prefill")
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample_rate(pcase, rows, "prefill")
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"fp64 oracle, {len(rows)} of {total_rows} query rows (every {stride}th) of {pc.name} "
+              f"per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": pc.name, "B": pc.B, "H": pc.H, "H_kv": pc.H_kv, "N_q": pc.N_q,
+                       "N_kv": pc.N_kv, "d": pc.d, "causal": pc.causal, "window": pc.window},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.default_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import tiled_attention_flashattention_gb300 as gb
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from tiled_attention_flashattention_gb300 import _build
+    _build.build()
+    gb.load_library()
+
+    pc = wl.WORKLOADS[args.workload]
+    dc = wl.WORKLOADS[args.decode_workload]
+    # per-rank inputs: independent shards (weak scaling), seeded per rank
+    pc_r = wl.PrefillCase(**{**pc.__dict__, "seed": pc.seed + 1000 * rank})
+    dc_r = wl.MlaCase(**{**dc.__dict__, "seed": dc.seed + 1000 * rank})
+    Qh, Kh, Vh = wl.prefill_inputs(pc_r)
+    dec_h = wl.mla_inputs(dc_r)
+    Q, K, V = (x.to(dev) for x in (Qh, Kh, Vh))
+    Qn, Qp, KV, Kp = (x.to(dev) for x in dec_h)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(pc.B, pc.H, pc.N_q, dtype=torch.float32, device=dev)
+    Od = torch.empty(dc.B, dc.H, dc.d_c, dtype=torch.bfloat16, device=dev)
+    Ld = torch.empty(dc.B, dc.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, gb.mla_decode_workspace_bytes(dc.B, dc.H, dc.N_kv, dc.d_c)), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale_p, scale_d = pc.softmax_scale(), dc.softmax_scale()
+
+    def step(events=None):
+        flush.zero_()
+        if events:
+            events[0].record(stream)
+        gb.attn_fwd(Q, K, V, causal=pc.causal, window=pc.window, scale=scale_p, O=O, LSE=LSE)
+        if events:
+            events[1].record(stream)
+        gb.mla_decode(Qn, Qp, KV, Kp, scale=scale_d, O=Od, LSE=Ld, workspace=ws)
+        if events:
+            events[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    gb.check()
+    n_ev = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    clocks = sampler.stop()
+    gb.check()
+    t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3   # seconds
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_pre = max_over_ranks(t_pre, world)
+    t_dec = max_over_ranks(t_dec, world)
+
+    peaks, peak_src = load_peaks()
+    fl_p = prefill_flops(pc)
+    by_d = decode_bytes(dc)
+    pre_launch_s = t_pre / args.steps
+    dec_launch_s = t_dec / args.steps
+    tflops = fl_p * args.steps * world / t_pre / 1e12
+    gbs = by_d * args.steps * world / t_dec / 1e9
+    n_dec_launches = 2 if gb.mla_decode_workspace_bytes(dc.B, dc.H, dc.N_kv, dc.d_c) > 0 else 1
+
+    # ---- end to end through the public API: pinned host inputs -> device -> host result
+    e2e_steps = max(3, min(args.steps, 20))
+    Qh_p, Kh_p, Vh_p = (x.pin_memory() for x in (Qh, Kh, Vh))
+    dec_p = [x.pin_memory() for x in dec_h]
+    O_h = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    L_h = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+    Od_h = torch.empty(Od.shape, dtype=Od.dtype).pin_memory()
+    Ld_h = torch.empty(Ld.shape, dtype=Ld.dtype).pin_memory()
+    e2e_pre, e2e_dec = 0.0, 0.0
+    for k in range(e2e_steps + 1):
+        flush.zero_()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        Q.copy_(Qh_p, non_blocking=True)
+        K.copy_(Kh_p, non_blocking=True)
+        V.copy_(Vh_p, non_blocking=True)
+        gb.attn_fwd(Q, K, V, causal=pc.causal, window=pc.window, scale=scale_p, O=O, LSE=LSE)
+        O_h.copy_(O, non_blocking=True)
+        L_h.copy_(LSE, non_blocking=True)
+        e1.record(stream)
+        for dst, src in zip((Qn, Qp, KV, Kp), dec_p):
+            dst.copy_(src, non_blocking=True)
+        gb.mla_decode(Qn, Qp, KV, Kp, scale=scale_d, O=Od, LSE=Ld, workspace=ws)
+        Od_h.copy_(Od, non_blocking=True)
+        Ld_h.copy_(Ld, non_blocking=True)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        if k > 0:
+            e2e_pre += e0.elapsed_time(e1) / 1e3
+            e2e_dec += e1.elapsed_time(e2) / 1e3
+    gb.check()
+    e2e_pre = max_over_ranks(e2e_pre, world)
+    e2e_dec = max_over_ranks(e2e_dec, world)
+    h2d_p = sum(x.numel() * x.element_size() for x in (Qh, Kh, Vh))
+    d2h_p = O.numel() * 2 + LSE.numel() * 4
+    h2d_d = sum(x.numel() * x.element_size() for x in dec_h)
+    d2h_d = Od.numel() * 2 + Ld.numel() * 4
+
+    if rank != 0:
+        return
+    src_p = kernel_source_hash("attn_fwd.cu")
+    src_d = kernel_source_hash("mla_decode.cu")
+    roof_p = {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": tflops / world / peaks["bf16_tflops"],
+              "traffic": traffic_per_launch("attn_fwd_kernel", "attn_fwd.cu", pc.name),
+              "kernel": "attn_fwd_kernel<128>", "peak_source": f"{peak_src} bf16 dense (burst)",
+              "algorithmic_flops_per_launch": fl_p}
+    roof_d = {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+              "frac": gbs / world / peaks["hbm_gbs"],
+              "traffic": traffic_per_launch("mla_decode", "mla_decode.cu", dc.name),
+              "kernel": "mla_split_kernel + mla_combine_kernel", "peak_source": f"{peak_src} HBM copy",
+              "algorithmic_bytes_per_launch": by_d}
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": (t_pre + t_dec) / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": pc.name, "B": pc.B, "H": pc.H, "H_kv": pc.H_kv, "N_q": pc.N_q, "N_kv": pc.N_kv,
+                   "d": pc.d, "causal": pc.causal, "window": pc.window, "decode_workload": dc.name,
+                   "parallelism": f"independent shards x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MiB buffer overwritten between steps (outside the timed kernels)"},
+        "roofline": roof_p,
+        "decode": {"metric": "MLA-decode HBM GB/s", "value": gbs, "unit": "GB/s",
+                   "ms_per_launch": dec_launch_s * 1e3, "roofline": roof_d,
+                   "tflops": decode_flops(dc) * args.steps * world / t_dec / 1e12,
+                   "e2e": {"value": by_d * e2e_steps * world / e2e_dec / 1e9, "unit": "GB/s",
+                           "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": d2h_d}},
+        "e2e": {"value": fl_p * e2e_steps * world / e2e_pre / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": d2h_p},
+        "gpu_launches": args.steps * (1 + n_dec_launches),
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "kernel_source": {"attn_fwd": src_p, "mla_decode": src_d},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
+        line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(args, local):
+    """Launch only the selected kernel(s), warmup + steps times, for ncu captures."""
+    import tiled_attention_flashattention_gb300 as gb
+    from tiled_attention_flashattention_gb300 import _build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    gb.load_library()
+    if args.profile == "prefill":
+        pc = wl.WORKLOADS[args.workload]
+        Q, K, V = (x.to(dev) for x in wl.prefill_inputs(pc))
+        O = torch.empty_like(Q)
+        LSE = torch.empty(pc.B, pc.H, pc.N_q, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gb.attn_fwd(Q, K, V, causal=pc.causal, window=pc.window, scale=pc.softmax_scale(), O=O, LSE=LSE)
+    else:
+        dc = wl.WORKLOADS[args.decode_workload]
+        Qn, Qp, KV, Kp = (x.to(dev) for x in wl.mla_inputs(dc))
+        O = torch.empty(dc.B, dc.H, dc.d_c, dtype=torch.bfloat16, device=dev)
+        LSE = torch.empty(dc.B, dc.H, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, gb.mla_decode_workspace_bytes(dc.B, dc.H, dc.N_kv, dc.d_c)),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gb.mla_decode(Qn, Qp, KV, Kp, scale=dc.softmax_scale(), O=O, LSE=LSE, workspace=ws)
+    gb.check()
+    print(f"profile case {args.profile}: {args.warmup + args.steps} launches ok", flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=PREFILL, choices=[k for k, v in wl.WORKLOADS.items()
+                                                            if isinstance(v, wl.PrefillCase)])
+    ap.add_argument("--decode-workload", default=DECODE, choices=[k for k, v in wl.WORKLOADS.items()
+                                                                  if isinstance(v, wl.MlaCase)])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="only launch the selected kernel warmup+steps times (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup(args.gpus)
+    if args.profile:
+        run_profile_case(args, local)
+        return
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

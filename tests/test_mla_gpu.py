@@ -37,10 +37,12 @@ def test_parity(B, N_kv):
 
 
 def test_large_scores_force_rescaling():
+    # Ramp the RoPE keys (they enter the scores only, not the values): the row
+    # maximum keeps moving along the sequence while V stays N(0, 1).
     B, N_kv = 2, 2048
     Qn, Qp, KV, Kp = wl.random_mla(B, 128, N_kv, 512, 64, seed=9)
-    ramp = torch.linspace(0.2, 5.0, N_kv).view(1, N_kv, 1)
-    KV = (KV.float() * ramp).to(torch.bfloat16)
+    ramp = torch.linspace(0.5, 10.0, N_kv).view(1, N_kv, 1)
+    Kp = (Kp.float() * ramp).to(torch.bfloat16)
     O, LSE = run(Qn, Qp, KV, Kp)
     O_ref, L_ref = oracle.mla_decode(Qn, Qp, KV, Kp, SCALE)
     compare(O, LSE, O_ref, L_ref, what="ramp")
