@@ -27,6 +27,8 @@
 // writes O / l and its LSE to the workspace, and a small combine kernel merges
 // the pieces of each split sequence with the exact log-sum-exp rule
 // (TileLang 学习笔记, "Online Softmax 的关键", applied across key ranges).
+// Only the first and the last sequence of a cluster's range can be partial,
+// so the workspace holds two slots per cluster whatever B and N_kv are.
 //
 // Per CTA (256 threads): warp 0 issues TMA loads, warp 1 issues tcgen05 MMAs,
 // warps 4-7 (one thread per head) exchange partial scores, run the softmax and
@@ -80,7 +82,7 @@ struct Params {
     int B, N_kv, ntile;
     long long T;        // B * ntile
     int C;              // clusters
-    int max_seg;        // workspace slots per cluster
+    int max_seg;        // workspace slots per cluster (2: its first and last range)
     float c;            // scale * log2(e)
     int *status;
     uint64_t timeout_ns;
@@ -350,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool whole = (n == p.ntile);
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             const float lse = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
-            const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - b_first);
+            const size_t slot = static_cast<size_t>(cl) * 2 + (b == b_first ? 0 : 1);
 #pragma unroll 1
             for (int ch = 0; ch < kHalf / 32; ++ch) {
                 uint32_t o[32];
@@ -409,18 +411,18 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const Params p)
     if (c0 == c1) return;
     float mx = -INFINITY;
     for (int cl = c0; cl <= c1; ++cl) {
-        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        const size_t slot = static_cast<size_t>(cl) * 2 + (b == range_start(cl, p.T, p.C) / p.ntile ? 0 : 1);
         mx = fmaxf(mx, p.ws_LSE[slot * kH + h]);
     }
     float denom = 0.f;
     for (int cl = c0; cl <= c1; ++cl) {
-        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        const size_t slot = static_cast<size_t>(cl) * 2 + (b == range_start(cl, p.T, p.C) / p.ntile ? 0 : 1);
         denom += expf(p.ws_LSE[slot * kH + h] - mx);
     }
     const float lse = mx + logf(denom);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int cl = c0; cl <= c1; ++cl) {
-        const size_t slot = static_cast<size_t>(cl) * p.max_seg + (b - range_start(cl, p.T, p.C) / p.ntile);
+        const size_t slot = static_cast<size_t>(cl) * 2 + (b == range_start(cl, p.T, p.C) / p.ntile ? 0 : 1);
         const float w = expf(p.ws_LSE[slot * kH + h] - lse);
         const float4 v = reinterpret_cast<const float4 *>(p.ws_O + (slot * kH + h) * kDc)[threadIdx.x];
         acc.x += w * v.x;
@@ -475,8 +477,7 @@ Plan make_plan(int B, int N_kv, int clusters)
     pl.ntile = (N_kv + kBN - 1) / kBN;
     pl.T = static_cast<long long>(B) * pl.ntile;
     pl.C = static_cast<int>(std::min<long long>(clusters, pl.T));
-    const long long per = (pl.T + pl.C - 1) / pl.C;
-    pl.max_seg = static_cast<int>((per + pl.ntile - 1) / pl.ntile) + 1;
+    pl.max_seg = 2;
     pl.slots = static_cast<size_t>(pl.C) * pl.max_seg;
     return pl;
 }
