@@ -113,6 +113,36 @@ int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, cons
                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point; it is a
+ * convenience of this library.
+ *
+ * Why: some callers cannot call cudaMalloc when they call this function -- a
+ * serving loop whose device memory is planned up front and must not grow, a
+ * caller that must not synchronise the device (allocating and freeing may),
+ * or a plain C caller without an allocator of its own.  This entry point does
+ * the same computation as mla_decode, with the same arguments minus the
+ * workspace, and allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  The split-KV partial results go to a scratch array built
+ * into the library instead: 42,024,960 bytes, enough for every shape on GPUs
+ * with up to 160 SMs, held by every GPU that loads the library until the
+ * process exits.  If the current device would need more scratch than that,
+ * the call returns GBATTN_ERR_WORKSPACE and enqueues nothing.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * scratch array, with that device current.  Make that first call before any
+ * stream capture on the device.
+ *
+ * All calls share the one scratch array, which keeps the contents of the last
+ * call; nothing in it needs to start at zero.  Calls whose kernels overlap on
+ * the GPU (for example on two streams) race on the scratch and give wrong
+ * results: serialise them, or use mla_decode with one workspace per stream.
+ */
+int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                       void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                       void *stream);
+
+/*
  * gbattn_check -- synchronise `stream`, then read and clear the device status
  * word of the current device.  Returns GBATTN_OK, GBATTN_ERR_TIMEOUT if a
  * kernel's bounded wait ran out since the last check, or GBATTN_ERR_LAUNCH if

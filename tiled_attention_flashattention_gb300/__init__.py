@@ -16,7 +16,7 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "mla_decode", "mla_decode_workspace_bytes", "check", "selftest_umma",
+__all__ = ["attn_fwd", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_noalloc", "check", "selftest_umma",
            "set_wait_timeout_ns", "GbattnError", "library_path", "load_library"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +55,8 @@ def load_library():
         lib.mla_decode_workspace_bytes.restype = SZ
         lib.mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
         lib.mla_decode.restype = I
+        lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
+        lib.mla_decode_noalloc.restype = I
         lib.gbattn_check.argtypes = [P]
         lib.gbattn_check.restype = I
         lib.gbattn_last_error.argtypes = []
@@ -161,6 +163,38 @@ def mla_decode(Q_nope, Q_pe, KV_latent, K_pe, scale: float | None = None, O=None
     rc = lib.mla_decode(_ptr(Q_nope), _ptr(Q_pe), _ptr(KV_latent), _ptr(K_pe), _ptr(O), _ptr(LSE),
                         B, H, N_kv, d_c, d_r, float(scale), _ptr(workspace), workspace.numel(),
                         ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def mla_decode_noalloc(Q_nope, Q_pe, KV_latent, K_pe, scale: float | None = None, O=None, LSE=None,
+                       stream=None):
+    """MLA decode through the library's built-in scratch: no workspace argument.
+
+    For callers that cannot allocate device memory at call time (a fixed
+    device-memory plan, no device synchronisation allowed).  The C call
+    allocates nothing; pass preallocated O and LSE so that this wrapper does
+    not allocate them with torch either.  Calls whose kernels overlap on the
+    GPU race on the shared scratch, so serialise them.
+    """
+    lib = load_library()
+    B, H, d_c = Q_nope.shape
+    d_r = Q_pe.shape[-1]
+    N_kv = KV_latent.shape[1]
+    _need(Q_nope, "Q_nope", torch.bfloat16, None)
+    _need(Q_pe, "Q_pe", torch.bfloat16, (B, H, d_r))
+    _need(KV_latent, "KV_latent", torch.bfloat16, (B, N_kv, d_c))
+    _need(K_pe, "K_pe", torch.bfloat16, (B, N_kv, d_r))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_c + d_r)
+    if O is None:
+        O = torch.empty((B, H, d_c), dtype=torch.bfloat16, device=Q_nope.device)
+    if LSE is None:
+        LSE = torch.empty((B, H), dtype=torch.float32, device=Q_nope.device)
+    _need(O, "O", torch.bfloat16, (B, H, d_c))
+    _need(LSE, "LSE", torch.float32, (B, H))
+    rc = lib.mla_decode_noalloc(_ptr(Q_nope), _ptr(Q_pe), _ptr(KV_latent), _ptr(K_pe), _ptr(O), _ptr(LSE),
+                                B, H, N_kv, d_c, d_r, float(scale), ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return O, LSE
 

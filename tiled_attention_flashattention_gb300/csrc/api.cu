@@ -194,6 +194,33 @@ extern "C" int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_l
     return rc;
 }
 
+extern "C" int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_latent,
+                                  const void *K_pe, void *O, float *LSE, int B, int H, int N_kv, int d_c,
+                                  int d_r, float scale, void *stream)
+{
+    g_err.clear();
+    if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_noalloc: need B, H, N_kv, d_c >= 1 and d_r >= 0");
+    if (!valid_scale(scale))
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_noalloc: scale must be finite and > 0");
+    if (d_c != 512 || d_r != 64 || H != 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_noalloc: supports d_c = 512, d_r = 64, H = 128");
+    if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_noalloc: problem too large");
+    if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_noalloc: null tensor pointer");
+    if (!aligned16(Q_nope) || !aligned16(Q_pe) || !aligned16(KV_latent) || !aligned16(K_pe) || !aligned16(O) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return fail(GBATTN_ERR_ALIGNMENT, "mla_decode_noalloc: tensors must be 16-byte aligned (LSE 4-byte)");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    std::string err;
+    rc = launch_mla_decode_noalloc(Q_nope, Q_pe, KV_latent, K_pe, O, LSE, B, H, N_kv, d_c, d_r, scale, env, err);
+    if (rc != GBATTN_OK) g_err = err;
+    return rc;
+}
+
 extern "C" int gbattn_check(void *stream)
 {
     g_err.clear();

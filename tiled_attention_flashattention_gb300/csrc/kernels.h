@@ -31,6 +31,12 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
                       void *workspace, size_t workspace_bytes, const LaunchEnv &env,
                       std::string &err);
 
+// MLA decode through the library's built-in scratch instead of a workspace
+// (mla_decode_noalloc); allocates nothing.
+int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                              void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                              const LaunchEnv &env, std::string &err);
+
 // Tensor-core layout self test (gbattn_selftest_umma).
 int launch_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
                          float *O, const LaunchEnv &env, std::string &err);

@@ -35,6 +35,8 @@
 // the epilogue.  TMEM: O half [0, 256), score tiles S0 [256, 320) and
 // S1 [320, 384) (double-buffered; P overwrites the first 32 columns).
 #include <cmath>
+#include <cstdio>
+#include <mutex>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -487,7 +489,70 @@ size_t plan_bytes(const Plan &pl)
     return pl.slots * kH * kDc * sizeof(float) + pl.slots * kH * sizeof(float);
 }
 
+// ---------------------------------------------------------------------------
+// Built-in scratch for mla_decode_noalloc.
+//
+// Some callers cannot allocate device memory at call time: code running under
+// a fixed device-memory plan that must not grow (a serving loop), a caller
+// that must not synchronise the device (cudaMalloc and cudaFree may), or a
+// plain C caller with no allocator of its own.  For them the split-KV partial
+// results live in this fixed array instead of a caller-provided workspace.
+// It is sized for the largest plan this kernel makes on GPUs with up to 160
+// SMs: 80 two-CTA clusters x 2 partial slots x (128 x 512 fp32 O + 128 fp32
+// LSE) = 42,024,960 bytes.  Every GPU that loads the library holds it until
+// the process exits.
+constexpr size_t kNoAllocMaxClusters = 80;
+constexpr size_t kNoAllocScratchBytes =
+    kNoAllocMaxClusters * 2 * (static_cast<size_t>(kH) * kDc * sizeof(float) + kH * sizeof(float));
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 }  // namespace
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current (in host code the symbol itself is only
+// a host-side stand-in, not a device address).
+static void *noalloc_scratch_ptr(std::string &err)
+{
+    static std::mutex mu;
+    static void *ptrs[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        err = std::string("mla_decode_noalloc: cudaGetDevice: ") + cudaGetErrorString(e);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            err = std::string("mla_decode_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                              void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                              const LaunchEnv &env, std::string &err)
+{
+    void *scratch = noalloc_scratch_ptr(err);
+    if (!scratch) return 5;
+    const size_t need = plan_bytes(make_plan(B, N_kv, resident_clusters(env.num_sms)));
+    if (need > kNoAllocScratchBytes) {
+        char buf[220];
+        snprintf(buf, sizeof buf,
+                 "mla_decode_noalloc: this device needs %zu bytes of split-KV scratch, more than the "
+                 "built-in maximum of %zu bytes; use mla_decode with a workspace",
+                 need, kNoAllocScratchBytes);
+        err = buf;
+        return 4;
+    }
+    return launch_mla_decode(Q_nope, Q_pe, KV_latent, K_pe, O, LSE, B, H, N_kv, d_c, d_r, scale, scratch,
+                             kNoAllocScratchBytes, env, err);
+}
 
 size_t mla_workspace_bytes(int B, int H, int N_kv, int d_c, int num_sms)
 {
