@@ -214,26 +214,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
             const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
             // S_t = Q_t K^T: K-major A and B, 16 bf16 (32 B) per MMA along d.
+            const uint64_t qdesc[2] = {smem_desc_sw128(sQa, 16, 1024),
+                                       smem_desc_sw128(sQa + C::kTileBytes, 16, 1024)};
             auto issue_S = [&](int t, int slot) {
+                const uint64_t ad = qdesc[t];
+                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes, 16, 1024);
+                umma_ss(tbase + C::col_s(t), ad, bd, idS, 0u);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 1; k < D / 16; ++k) {
                     const uint32_t koff = (k / 4) * kChunkBytes + (k % 4) * 32;
-                    const uint64_t a = smem_desc_sw128(sQa + t * C::kTileBytes + koff, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes + koff, 16, 1024);
-                    umma_ss(tbase + C::col_s(t), a, bd, idS, k > 0 ? 1u : 0u);
+                    umma_ss(tbase + C::col_s(t), desc_advance(ad, koff), desc_advance(bd, koff), idS, 1u);
                 }
             };
             // O_t += P_t V: P from TMEM (8 columns per 16 keys), V N-major
             // (64-wide d chunks 16 KB apart, 16 keys = 2048 B per MMA).
             bool started[2] = {false, false};
             auto issue_PV = [&](int t, int slot) {
+                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes, kChunkBytes, 1024);
+                umma_ts(tbase + C::col_o(t), tbase + C::col_s(t), bd, idPV, started[t] ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < kBN / 16; ++k) {
-                    const uint64_t bd =
-                        smem_desc_sw128(ringa + slot * C::kTileBytes + k * 2048, kChunkBytes, 1024);
-                    umma_ts(tbase + C::col_o(t), tbase + C::col_s(t) + k * 8, bd, idPV,
-                            (started[t] || k > 0) ? 1u : 0u);
-                }
+                for (int k = 1; k < kBN / 16; ++k)
+                    umma_ts(tbase + C::col_o(t), tbase + C::col_s(t) + k * 8, desc_advance(bd, k * 2048), idPV, 1u);
                 started[t] = true;
             };
             auto in_rng = [&](int t, int j) { return j >= rng[t].lo && j < rng[t].hi; };

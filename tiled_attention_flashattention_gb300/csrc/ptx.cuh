@@ -145,6 +145,19 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Same load, written to the same shared-memory offset of every CTA in
+// cta_mask (this cluster), completing bytes on the mbarrier at the same
+// offset in each of them.
+__device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                                      int y, int z, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
                                             int y)
 {
@@ -223,6 +236,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Descriptor of the same operand shifted by byte_off bytes (a multiple of 16):
+// only the start-address field changes.  Shared memory is below 256 KB, so the
+// 14-bit field never carries into the next one.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t byte_off)
+{
+    return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), A/B major-ness (bit 15/16: 0 = K-major,
 // 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -262,6 +283,17 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// As umma_commit, arriving on the mbarrier at the same offset in every CTA of
+// cta_mask (this cluster).
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 
