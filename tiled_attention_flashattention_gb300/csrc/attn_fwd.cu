@@ -45,6 +45,11 @@ constexpr int kThreads = 384;
 constexpr int kChunkBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.693147180559945309f;
+// Registers per thread after the per-role split (setmaxnreg): warpgroup 0
+// (producer, MMA issuer, two idle warps) gives registers to the two softmax
+// warpgroups, which hold a 128-float score row per thread.  128 * 104 +
+// 256 * 200 = 64,512, the 384 * 168 registers the block is launched with.
+constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
 
 template <int D>
 struct Cfg {
@@ -168,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // =================== TMA producer ===================
+        regs_dec<kRegsLow>();
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // =================== tensor-core issuer ===================
+        regs_dec<kRegsLow>();
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
@@ -300,8 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
             mbar_wait(&c.drain, 0, drain);
         }
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        regs_dec<kRegsLow>();
+    } else {
         // =================== softmax: one thread per query row ===================
+        regs_inc<kRegsHigh>();
         const int t = (warp - 4) / 4;
         const int quad = warp % 4;                 // TMEM lanes [32*quad, 32*quad+32)
         const int row = r0[t] + quad * 32 + lane;
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             uint32_t sr[128];
-            tmem_ld_x128(tS, sr);
+            tmem_ld_4x32(tS, sr);
             float s[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
@@ -349,19 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool move = mx > m_ref + thr;
             const float new_ref = move ? mx : m_ref;
             const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
-            l *= alpha;
-            if (n > 0 && __any_sync(0xffffffffu, move)) {
-                // O_t already holds the PV products of earlier tiles (their
-                // completion is covered by this tile's S commit): rescale it.
-#pragma unroll 1
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + ch * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_x32(tO + ch * 32, o);
-                }
-            }
             m_ref = new_ref;
             const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
             float sum = 0.f;
@@ -377,7 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_x16(tS + q * 16, pk);
             }
-            l += sum;
+            l = l * alpha + sum;
+            if (n > 0 && __any_sync(0xffffffffu, move)) {
+                // O_t already holds the PV products of earlier tiles (their
+                // completion is covered by this tile's S commit); rescale it
+                // before this tile's PV, which waits for p_full below.
+#pragma unroll 1
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + ch * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_x32(tO + ch * 32, o);
+                }
+            }
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&c.p_full[t]);
