@@ -11,14 +11,16 @@
 //
 // GB300 mapping.  The fp32 output accumulator of 128 heads x 512 latent dims
 // fills one SM's whole tensor memory, so a pair of CTAs (a 2-CTA cluster)
-// shares each work item and splits the output: CTA r owns O[:, 256r, 256r+256).
-// Each CTA computes the full 576-dim score tile itself (the contraction is
-// not split, so no partial scores cross SMs; distributed shared memory moves
-// only ~17 B/cycle per direction on this part, far too little for a 32 KB
-// partial-score swap per 64 keys).  The KV tile is still fetched once per
-// cluster: each CTA issues half of its TMA boxes with cluster multicast, so
-// both CTAs receive the whole tile, and a stage is refilled only after both
-// CTAs' tensor cores have released it (multicast tcgen05.commit).
+// shares each work item and splits both the contraction and the output:
+//   CTA 0 holds latent dims [0, 256): its Q part and KV tiles cover those
+//         dims; it computes the partial score over them and owns O[:, 0:256);
+//   CTA 1 holds latent dims [256, 512) plus the 64 RoPE dims, computes the
+//         partial score over those 320 dims and owns O[:, 256:512).
+// Every KV byte is read from HBM by exactly one CTA.  The two fp32 partial
+// score tiles (128 heads x 64 keys, 32 KB) are swapped with one bulk copy per
+// CTA per tile (TMA engine, shared memory to the peer's shared memory), so
+// both CTAs hold the same full score tile and run the same online softmax;
+// each then multiplies P by its own latent half (V = KV_latent).
 //
 // Work split: the B * ceil(N_kv / 64) key tiles are cut into one contiguous
 // range per cluster (as many clusters as fit on the GPU at once).  A range
@@ -29,17 +31,18 @@
 // Only the first and the last sequence of a cluster's range can be partial,
 // so the workspace holds two slots per cluster whatever B and N_kv are.
 //
-// Per CTA (256 threads, one CTA per SM):
-//   warp 0      TMA producer: this CTA's half of every 64-key tile (latent
-//               chunks 0-4 or 5-7 plus the RoPE chunk), multicast, 2 stages;
-//               the shared-memory part of Q once per sequence;
-//   warp 1      tcgen05 issuer: S = Q K^T (dims 0-383 with Q from TMEM, dims
-//               384-575 with Q from shared memory), then O += P V_half;
-//   warps 4-7   one thread per head: this sequence's Q dims 0-383 into TMEM,
-//               online softmax, P (bf16) to shared memory, O rescaling,
-//               epilogue.
-// TMEM: O half [0, 256), S [256, 320), Q dims 0-383 [320, 512) (two bf16
-// per column).
+// Per CTA (384 threads, one CTA per SM):
+//   warp 0      TMA producer: this CTA's dims of each 64-key tile, 4 stages;
+//   warp 1      tcgen05 issuer: S_part = Q_part K_part^T with Q from TMEM,
+//               then O_half += P V_half with P from TMEM (N = 256);
+//   warps 4-7   exchange (one thread per head): this sequence's Q part into
+//               TMEM; per tile read S_part, send it to the peer, add the
+//               peer's part, hand the full score row to the softmax warps;
+//   warps 8-11  softmax (one thread per head): online softmax, P (bf16) into
+//               TMEM, O rescaling, epilogue.
+// The exchange of tile j+1 overlaps the softmax of tile j; the score buffer
+// is released as soon as the exchange warps have read it.
+// TMEM: O half [0, 256), S [256, 320), P [320, 352), Q part [352, 512).
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -53,21 +56,19 @@ namespace {
 constexpr int kH = 128;                   // heads per tile (MMA M)
 constexpr int kBN = 64;                   // keys per tile
 constexpr int kDc = 512;
-constexpr int kHalf = 256;                // latent dims of O owned by one CTA
+constexpr int kHalf = 256;                // latent dims owned by one CTA
 constexpr int kKvChunk = kBN * 128;       // [64 keys x 64 dims] bf16, one TMA box
-constexpr int kChunks = 9;                // 8 latent chunks + 1 RoPE chunk per tile
-constexpr int kStageBytes = kChunks * kKvChunk;
-constexpr int kStages = 2;
-constexpr int kQChunk = kH * 128;         // [128 heads x 64 dims] bf16
-constexpr int kQSmemChunks = 3;           // latent dims 384-511 and the RoPE dims
-constexpr int kQTmemChunks = 6;           // latent dims 0-383
-constexpr int kPBytes = kH * 128;         // P tile [128 heads x 64 keys] bf16, 128-byte rows
-constexpr int kThreads = 256;
+constexpr int kMaxChunks = 5;             // contraction chunks of CTA 1 (4 latent + RoPE)
+constexpr int kStageBytes = kMaxChunks * kKvChunk;
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 256;           // S (one buffer of 64 columns)
-constexpr uint32_t kColQ = 320;
-constexpr uint16_t kBothCtas = 0x3;
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColP = 320;
+constexpr uint32_t kColQ = 352;
+constexpr int kXBytes = kH * kBN * 4;     // one partial score tile (fp32)
+constexpr uint32_t kBarX = 1, kBarS = 2;  // named barriers of the exchange / softmax warps
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -75,19 +76,20 @@ struct Ctl {
     uint64_t q_full, q_empty;
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full, s_free;
-    uint64_t p_full[2], pfree[2];
+    uint64_t xfull, xfree, sready;
+    uint64_t p_full, pfree;
     uint64_t o_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes +
-                              static_cast<size_t>(kQSmemChunks) * kQChunk + 2 * static_cast<size_t>(kPBytes) +
-                              sizeof(Ctl);
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * kStageBytes + 2 * static_cast<size_t>(kXBytes) + sizeof(Ctl);
 
 struct Params {
     const __nv_bfloat16 *Qn;   // [B][128][512]
+    const __nv_bfloat16 *Qp;   // [B][128][64]
     __nv_bfloat16 *O;
     float *LSE;
     float *ws_O;        // [slots][128][512] fp32, O / l of partial ranges
@@ -114,39 +116,40 @@ __host__ __device__ __forceinline__ int cluster_of_tile(long long x, long long T
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_split_kernel(const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp,
-                     const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
+    mla_split_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
                      const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sKV = smem;                                   // [stage][chunk][32 keys][128 B]
-    uint8_t *sQ = sKV + kStages * kStageBytes;             // [3][128 heads][128 B]
-    uint8_t *sP = sQ + kQSmemChunks * kQChunk;             // [2][128 heads][128 B] (first 64 B used)
-    Ctl &c = *reinterpret_cast<Ctl *>(sP + 2 * kPBytes);
+    uint8_t *sKV = smem;                                   // [stage][chunk][64 keys][128 B]
+    uint8_t *sSend = sKV + kStages * kStageBytes;          // [128 rows][256 B] fp32, swizzled
+    uint8_t *sRecv = sSend + kXBytes;                      // [128 rows][256 B] fp32, swizzled
+    Ctl &c = *reinterpret_cast<Ctl *>(sRecv + kXBytes);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int cl = blockIdx.x / 2;
     const long long t_begin = range_start(cl, p.T, p.C), t_end = range_start(cl + 1, p.T, p.C);
-    const int dim0 = static_cast<int>(rank) * kHalf;       // O columns owned by this CTA
+    const int nch = rank == 0 ? 4 : 5;              // contraction chunks of this CTA
+    const int dim0 = static_cast<int>(rank) * kHalf;
     const int b_first = static_cast<int>(t_begin / p.ntile);
     const int b_last = t_end > t_begin ? static_cast<int>((t_end - 1) / p.ntile) : b_first - 1;
 
     if (threadIdx.x == 0) {
-        mbar_init(&c.q_full, 128 + 1);      // 128 softmax threads (TMEM part) + producer (TMA part)
+        mbar_init(&c.q_full, 128);
         mbar_init(&c.q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&c.full[s], 1);
-            mbar_init(&c.empty[s], 2);      // released by both CTAs' tensor cores
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&c.p_full[i], 128);
-            mbar_init(&c.pfree[i], 1);
+            mbar_init(&c.empty[s], 1);
         }
         mbar_init(&c.s_full, 1);
         mbar_init(&c.s_free, 128);
+        mbar_init(&c.xfull, 1);       // this CTA's expect_tx arrive + the peer's 32 KB
+        mbar_init(&c.xfree, 1);       // remote arrive: the peer's receive buffer is free
+        mbar_init(&c.sready, 128);
+        mbar_init(&c.p_full, 128);
+        mbar_init(&c.pfree, 1);
         mbar_init(&c.o_empty, 128);
         mbar_init(&c.drain, 1);
         c.abort = 0;
@@ -158,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
     }
     __syncthreads();
-    cluster_sync_all();            // the peer's barriers exist before any multicast lands
+    cluster_sync_all();            // the peer's barriers exist before any remote arrive or copy
     tc_fence_after_sync();
     const uint32_t tbase = c.tmem_base;
     const WaitCtl ctl{&c.abort, p.status, p.timeout_ns};
@@ -166,42 +169,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // =================== TMA producer ===================
         if (lane == 0) {
-            tma_prefetch_desc(&tmQn);
-            tma_prefetch_desc(&tmQp);
             tma_prefetch_desc(&tmKV);
             tma_prefetch_desc(&tmKp);
             bool ok = true;
-            int it = 0, seg = 0, q_issued = 0;
-            const int ch_lo = rank == 0 ? 0 : 5, ch_hi = rank == 0 ? 5 : kChunks;   // this CTA's boxes
-            for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
+            int it = 0;
+            const uint32_t kvbytes = nch * kKvChunk;
+            for (int b = b_first; b <= b_last && ok; ++b) {
                 const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
                 const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
-                if (seg > 0 && !(ok = mbar_wait(&c.q_empty, (seg - 1) & 1, ctl))) break;
-                mbar_arrive_expect_tx(&c.q_full, kQSmemChunks * kQChunk);
-                tma_load_3d(sQ, &tmQn, &c.q_full, 384, 0, b);
-                tma_load_3d(sQ + kQChunk, &tmQn, &c.q_full, 448, 0, b);
-                tma_load_3d(sQ + 2 * kQChunk, &tmQp, &c.q_full, 0, 0, b);
-                ++q_issued;
                 for (long long x = x0; x < x1; ++x) {
                     const int key0 = static_cast<int>(x - static_cast<long long>(b) * p.ntile) * kBN;
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
-                    mbar_arrive_expect_tx(&c.full[s], kStageBytes);
-                    for (int ch = ch_lo; ch < ch_hi; ++ch) {
-                        if (ch < 8)
-                            tma_load_3d_multicast(dst + ch * kKvChunk, &tmKV, &c.full[s], ch * 64, key0, b, kBothCtas);
-                        else
-                            tma_load_3d_multicast(dst + ch * kKvChunk, &tmKp, &c.full[s], 0, key0, b, kBothCtas);
-                    }
+                    mbar_arrive_expect_tx(&c.full[s], kvbytes);
+                    for (int ch = 0; ch < 4; ++ch)
+                        tma_load_3d(dst + ch * kKvChunk, &tmKV, &c.full[s], dim0 + ch * 64, key0, b);
+                    if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, key0, b);
                     ++it;
                 }
             }
             if (!ok) {
                 volatile int no_abort = 0;
                 const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
-                if (q_issued > 0) mbar_wait(&c.q_full, (q_issued - 1) & 1, drain);
                 for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
                     mbar_wait(&c.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, drain);
             }
@@ -211,26 +202,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kH, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kH, kHalf, false, true);
-            const uint32_t sKVa = smem_u32(sKV), sPa = smem_u32(sP);
-            const uint64_t qd = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint32_t sKVa = smem_u32(sKV);
             bool ok = true;
             int it = 0, seg = 0;
             uint32_t g = 0;      // global tile counter
-            // O_half += P V_half for tile gp: P from shared memory (K-major,
-            // 16 keys = 32 B per MMA); V = this CTA's latent chunks of stage
-            // sp read N-major (64-dim blocks 4 KB apart, 16 keys = 2 KB).
+            // O_half += P V_half for tile gp: P from TMEM (8 columns per 16
+            // keys); V = the latent chunks of stage sp read N-major (64-dim
+            // blocks 8 KB apart, 16 keys = 2 KB per MMA).
             auto issue_pv = [&](uint32_t gp, int sp, bool first) -> bool {
-                if (!mbar_wait(&c.p_full[gp & 1], (gp >> 1) & 1u, ctl)) return false;
+                if (!mbar_wait(&c.p_full, gp & 1u, ctl)) return false;
                 if (first && seg > 0 && !mbar_wait(&c.o_empty, (seg - 1) & 1, ctl)) return false;
                 tc_fence_after_sync();
-                const uint64_t pd = smem_desc_sw128(sPa + (gp & 1) * kPBytes, 16, 1024);
-                const uint64_t vd = smem_desc_sw128(sKVa + sp * kStageBytes + (4 * rank) * kKvChunk, kKvChunk, 1024);
-                umma_ss(tbase + kColO, pd, vd, idPV, first ? 0u : 1u);
+                const uint64_t vd = smem_desc_sw128(sKVa + sp * kStageBytes, kKvChunk, 1024);
+                umma_ts(tbase + kColO, tbase + kColP, vd, idPV, first ? 0u : 1u);
 #pragma unroll
                 for (int k = 1; k < kBN / 16; ++k)
-                    umma_ss(tbase + kColO, desc_advance(pd, k * 32), desc_advance(vd, k * 2048), idPV, 1u);
-                umma_commit(&c.pfree[gp & 1]);
-                umma_commit_multicast(&c.empty[sp], kBothCtas);
+                    umma_ts(tbase + kColO, tbase + kColP + k * 8, desc_advance(vd, k * 2048), idPV, 1u);
+                umma_commit(&c.pfree);
+                umma_commit(&c.empty[sp]);
                 return true;
             };
             for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
@@ -242,21 +231,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < n; ++i) {
                     const int s = it % kStages;
                     if (!(ok = mbar_wait(&c.full[s], static_cast<uint32_t>(it / kStages) & 1u, ctl))) break;
-                    if (g >= 1 && !(ok = mbar_wait(&c.s_free, (g - 1) & 1u, ctl))) break;
+                    if (g > 0 && !(ok = mbar_wait(&c.s_free, (g - 1) & 1u, ctl))) break;
                     tc_fence_after_sync();
-                    const uint32_t dS = tbase + kColS;
+                    // S_part = Q_part K_part^T: Q from TMEM (8 columns per 16 dims).
                     const uint64_t kvd = smem_desc_sw128(sKVa + s * kStageBytes, 16, 1024);
-                    // dims 0-383: Q from TMEM (8 columns per 16 dims)
-                    umma_ts(dS, tbase + kColQ, kvd, idS, 0u);
-#pragma unroll
-                    for (int k = 1; k < kQTmemChunks * 4; ++k)
-                        umma_ts(dS, tbase + kColQ + k * 8, desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idS,
-                                1u);
-                    // dims 384-575: Q from shared memory
-#pragma unroll
-                    for (int k = 0; k < kQSmemChunks * 4; ++k)
-                        umma_ss(dS, desc_advance(qd, (k / 4) * kQChunk + (k % 4) * 32),
-                                desc_advance(kvd, (kQTmemChunks + k / 4) * kKvChunk + (k % 4) * 32), idS, 1u);
+                    umma_ts(tbase + kColS, tbase + kColQ, kvd, idS, 0u);
+                    for (int k = 1; k < nch * 4; ++k)
+                        umma_ts(tbase + kColS, tbase + kColQ + k * 8,
+                                desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idS, 1u);
                     umma_commit(&c.s_full);
                     if (i == n - 1) umma_commit(&c.q_empty);
                     if (i > 0 && !(ok = issue_pv(g - 1, prev_stage, i == 1))) break;
@@ -271,14 +253,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
             mbar_wait(&c.drain, 0, drain);
         }
-    } else if (warp >= 4) {
-        // =================== Q load, softmax, epilogue (one thread per head) ===================
+    } else if (warp >= 4 && warp < 8) {
+        // =================== Q load + partial-score exchange (one thread per head) ===================
         const int quad = warp - 4;
         const int row = quad * 32 + lane;
+        const bool leader = threadIdx.x == 128;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tO = tbase + lane_base + kColO;
-        const float cexp = p.c;
-        const float thr = kRescaleLog2 / cexp;
+        const uint32_t swz = static_cast<uint32_t>(row & 15);
+        const uint32_t peer_recv = mapa_shared(smem_u32(sRecv), peer);
+        const uint32_t peer_xfull = mapa_shared(smem_u32(&c.xfull), peer);
+        float4 *send_row = reinterpret_cast<float4 *>(sSend + row * 256);
+        float4 *recv_row = reinterpret_cast<float4 *>(sRecv + row * 256);
         bool ok = true;
         uint32_t g = 0;
         int seg = 0;
@@ -286,11 +271,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
             const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
             const int n = static_cast<int>(x1 - x0);
-            // Q dims 0-383 of this head into TMEM (two bf16 per column).
-            if (seg > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(&c.q_empty, (seg - 1) & 1, ctl)))) break;
-            const uint4 *qn = reinterpret_cast<const uint4 *>(p.Qn + (static_cast<size_t>(b) * kH + row) * kDc);
+            // This CTA's part of the query row into TMEM (two bf16 per column).
+            if (seg > 0 && !(ok = barrier_and(kBarX, 128, mbar_wait(&c.q_empty, (seg - 1) & 1, ctl)))) break;
+            const uint4 *qn = reinterpret_cast<const uint4 *>(p.Qn + (static_cast<size_t>(b) * kH + row) * kDc + dim0);
 #pragma unroll 1
-            for (int ch = 0; ch < kQTmemChunks; ++ch) {
+            for (int ch = 0; ch < 4; ++ch) {
                 uint32_t r[32];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -302,41 +287,126 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_x32(tbase + lane_base + kColQ + ch * 32, r);
             }
+            if (rank == 1) {
+                const uint4 *qp = reinterpret_cast<const uint4 *>(p.Qp + (static_cast<size_t>(b) * kH + row) * 64);
+                uint32_t r[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 v = __ldg(qp + k);
+                    r[4 * k] = v.x;
+                    r[4 * k + 1] = v.y;
+                    r[4 * k + 2] = v.z;
+                    r[4 * k + 3] = v.w;
+                }
+                tmem_st_x32(tbase + lane_base + kColQ + 128, r);
+            }
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&c.q_full);
 
-            float m_ref = -INFINITY, l = 0.f;
             for (int i = 0; i < n; ++i, ++g) {
-                const uint32_t buf = g & 1;
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full, g & 1u, ctl)))) break;
+                if (!(ok = barrier_and(kBarX, 128, mbar_wait(&c.s_full, g & 1u, ctl)))) break;
                 tc_fence_after_sync();
-                uint32_t sr[kBN];
+                uint32_t sr[64];
                 tmem_ld_x64(tbase + lane_base + kColS, sr);
                 tc_fence_before_sync();
                 mbar_arrive(&c.s_free);
-                float s[kBN];
+                // The previous copy must have finished reading the send buffer.
+                if (leader && g > 0) bulk_wait_read_all();
+                named_barrier(kBarX, 128);
 #pragma unroll
-                for (int k = 0; k < kBN; ++k) s[k] = __uint_as_float(sr[k]);
+                for (int q = 0; q < 16; ++q)
+                    send_row[q ^ swz] = make_float4(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1]),
+                                                    __uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3]));
+                fence_proxy_async_smem();      // the copy engine reads the send buffer
+                named_barrier(kBarX, 128);
+                if (leader) {
+                    // The peer's receive buffer is free once its softmax warps read tile g - 1.
+                    bool got = (g == 0) || mbar_wait_cluster(&c.xfree, (g - 1) & 1u, ctl);
+                    if (got) {
+                        mbar_arrive_expect_tx(&c.xfull, kXBytes);   // this CTA's incoming tile
+                        bulk_copy_to_peer(peer_recv, sSend, kXBytes, peer_xfull);
+                        bulk_commit_group();
+                    }
+                }
+                if (!(ok = barrier_and(kBarX, 128, mbar_wait_cluster(&c.xfull, g & 1u, ctl)))) break;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float4 v = recv_row[q ^ swz];
+                    v.x += __uint_as_float(sr[4 * q]);
+                    v.y += __uint_as_float(sr[4 * q + 1]);
+                    v.z += __uint_as_float(sr[4 * q + 2]);
+                    v.w += __uint_as_float(sr[4 * q + 3]);
+                    recv_row[q ^ swz] = v;
+                }
+                mbar_arrive(&c.sready);
+            }
+        }
+        if (leader) bulk_wait_all();   // no copy of this CTA may still be writing to the peer
+    } else if (warp >= 8) {
+        // =================== softmax + epilogue (one thread per head) ===================
+        const int quad = warp - 8;
+        const int row = quad * 32 + lane;
+        const bool leader = threadIdx.x == 256;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tO = tbase + lane_base + kColO;
+        const float cexp = p.c;
+        const float thr = kRescaleLog2 / cexp;
+        const uint32_t swz = static_cast<uint32_t>(row & 15);
+        const uint32_t peer_xfree = mapa_shared(smem_u32(&c.xfree), peer);
+        const float4 *recv_row = reinterpret_cast<const float4 *>(sRecv + row * 256);
+        bool ok = true;
+        uint32_t g = 0;
+        int seg = 0;
+        for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
+            const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
+            const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+            const int n = static_cast<int>(x1 - x0);
+            float m_ref = -INFINITY, l = 0.f;
+            for (int i = 0; i < n; ++i, ++g) {
+                const bool got = mbar_wait(&c.sready, g & 1u, ctl);
+                float s[64];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 v = recv_row[q ^ swz];
+                    s[4 * q] = v.x;
+                    s[4 * q + 1] = v.y;
+                    s[4 * q + 2] = v.z;
+                    s[4 * q + 3] = v.w;
+                }
+                // all 128 rows read: the peer may send its next tile
+                if (!(ok = barrier_and(kBarS, 128, got))) break;
+                if (leader) mbar_arrive_remote(peer_xfree);
+
                 const int key0 = static_cast<int>(x0 + i - static_cast<long long>(b) * p.ntile) * kBN;
                 if (key0 + kBN > p.N_kv) {
 #pragma unroll
-                    for (int k = 0; k < kBN; ++k)
+                    for (int k = 0; k < 64; ++k)
                         if (key0 + k >= p.N_kv) s[k] = -INFINITY;
                 }
                 float mx = s[0];
 #pragma unroll
-                for (int k = 1; k < kBN; ++k) mx = fmaxf(mx, s[k]);
+                for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
                 const bool move = mx > m_ref + thr;
                 const float new_ref = move ? mx : m_ref;
                 const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
-                l *= alpha;
-                bool rescaled = false;
+                m_ref = new_ref;
+                const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
+                float sum = 0.f;
+                uint32_t pk[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
+                    const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
+                    sum += p0 + p1;
+                    pk[k] = pack_bf16x2(p0, p1);
+                }
+                l = l * alpha + sum;
+                // PV of the previous tile must be done: it read the P buffer,
+                // and O must be stable before it is rescaled.
+                if (g > 0 && !(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree, (g - 1) & 1u, ctl)))) break;
+                tc_fence_after_sync();
                 if (i > 0 && __any_sync(0xffffffffu, move)) {
-                    // O holds the PV products up to the previous tile; wait for the last one.
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.pfree[(g - 1) & 1], ((g - 1) >> 1) & 1u, ctl))))
-                        break;
-                    tc_fence_after_sync();
 #pragma unroll 1
                     for (int ch = 0; ch < kHalf / 32; ++ch) {
                         uint32_t o[32];
@@ -345,39 +415,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                         tmem_st_x32(tO + ch * 32, o);
                     }
-                    rescaled = true;
                 }
-                m_ref = new_ref;
-                const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-                // The P buffer of this tile was last read by PV(g - 2).
-                if (g >= 2 && !(ok = __all_sync(0xffffffffu, mbar_wait(&c.pfree[buf], ((g - 2) >> 1) & 1u, ctl))))
-                    break;
-                float sum = 0.f;
-                uint8_t *prow = sP + buf * kPBytes + row * 128;
-#pragma unroll
-                for (int q = 0; q < kBN / 8; ++q) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float p0 = ex2_approx(fmaf(s[8 * q + 2 * k], cexp, -base));
-                        const float p1 = ex2_approx(fmaf(s[8 * q + 2 * k + 1], cexp, -base));
-                        sum += p0 + p1;
-                        w[k] = pack_bf16x2(p0, p1);
-                    }
-                    *reinterpret_cast<uint4 *>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                l += sum;
-                if (rescaled) {
-                    tmem_st_wait();
-                    tc_fence_before_sync();
-                }
-                fence_proxy_async_smem();   // P is read by the tensor core (async proxy)
-                mbar_arrive(&c.p_full[buf]);
+                tmem_st_x32(tbase + lane_base + kColP, pk);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(&c.p_full);
             }
             if (!ok) break;
 
             // ---- epilogue of this range of sequence b (after its last PV)
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&c.pfree[(g - 1) & 1], ((g - 1) >> 1) & 1u, ctl)))) break;
+            if (!(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree, (g - 1) & 1u, ctl)))) break;
             tc_fence_after_sync();
             const bool whole = (n == p.ntile);
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
@@ -417,9 +464,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- teardown: no MMA or TMA of this CTA is in flight (drained above);
-    // the peer must be done sending into this CTA's shared memory and
-    // arriving on its barriers before either CTA exits.
+    // ---- teardown: no MMA, TMA or bulk copy of this CTA is in flight
+    // (drained above); the peer must be done with this CTA's shared memory
+    // before either CTA exits.
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
@@ -610,13 +657,12 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
         err = "mla_decode: workspace too small";
         return 4;
     }
-    CUtensorMap tqn, tqp, tkv, tkp;
-    if (!make_tma_bf16_3d(tqn, Q_nope, d_c, H, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, H, B, kH, err) ||
-        !make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) ||
-        !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err))
+    CUtensorMap tkv, tkp;
+    if (!make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) || !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err))
         return 5;
     Params p;
     p.Qn = static_cast<const __nv_bfloat16 *>(Q_nope);
+    p.Qp = static_cast<const __nv_bfloat16 *>(Q_pe);
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
     p.ws_O = static_cast<float *>(workspace);
@@ -633,7 +679,7 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     cudaError_t e = cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
-        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tqn, tqp, tkv, tkp, p);
+        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, p);
         e = cudaGetLastError();
     }
     bool split = false;   // does a cluster range boundary fall inside a sequence?

@@ -483,6 +483,57 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Bulk copy (TMA engine) of `bytes` bytes from this CTA's shared memory to
+// another CTA's shared memory (dst and bar are shared::cluster addresses from
+// mapa_shared); the bytes complete on that CTA's mbarrier.  Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                                  uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk copy of this thread has finished reading
+// its source.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Barrier over `count` threads (a multiple of 32) of this CTA, id 1..15.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier over `count` threads that also ANDs a flag across them: every
+// participant gets true only if all passed true.  Used to keep break
+// decisions uniform across a group of warps that share named barriers.
+__device__ __forceinline__ bool barrier_and(uint32_t id, uint32_t count, bool flag)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(flag ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Wait until every committed bulk copy of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier shared::cluster writes to it.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr)
