@@ -109,7 +109,8 @@ __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params p)
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -393,33 +394,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&c.p_full[t]);
         }
 
-        // ---- epilogue: O / l -> bf16, LSE
+        // ---- epilogue: O / l -> bf16, staged in this tile's Q buffer (free:
+        // o_final covers every MMA of the CTA that read it) in the
+        // 128-byte-swizzled layout of the O tensor map, then two TMA stores.
+        // LSE is a plain coalesced store.
         const size_t out_row = (static_cast<size_t>(b) * p.H + h) * p.N_q + row;
-        if (has[t] && ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&c.o_final[t], 0, ctl));
+        if (has[t]) {
+            ok = barrier_and(1 + t, 128, ok && mbar_wait(&c.o_final[t], 0, ctl));
             if (ok) {
                 tc_fence_after_sync();
                 const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+                uint8_t *stage = sQ + t * C::kTileBytes;
+                const int r = quad * 32 + lane;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
                     tmem_ld_x32(tO + ch * 32, o);
-                    uint4 v[4];
-                    uint32_t *w = reinterpret_cast<uint32_t *>(v);
+                    uint8_t *dst_row = stage + (ch / 2) * kChunkBytes + r * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                           __uint_as_float(o[2 * i + 1]) * inv_l);
-                    if (row_valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.O + out_row * D + ch * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[8 * k]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+                        const int c16 = (ch % 2) * 4 + k;          // 16-byte chunk within the 128-byte row
+                        *reinterpret_cast<uint4 *>(dst_row + ((c16 ^ (r & 7)) << 4)) = v;
                     }
                 }
                 if (row_valid)
                     p.LSE[out_row] = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
+                fence_proxy_async_smem();
+                named_barrier(1 + t, 128);
+                if (quad == 0 && lane == 0) {
+                    for (int ch = 0; ch < C::kChunks; ++ch)
+                        tma_store_3d(&tmO, stage + ch * kChunkBytes, ch * 64, r0[t], bh);
+                    bulk_commit_group();
+                    bulk_wait_all();        // stores complete before the CTA retires
+                }
             }
-        } else if (!has[t] && row_valid) {
+        } else if (row_valid) {
             // No key is visible to any row of this tile.
             uint4 *dst = reinterpret_cast<uint4 *>(p.O + out_row * D);
             for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -438,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
-           int grid, const LaunchEnv &env, std::string &err)
+int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+           const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
     static bool configured = false;   // per process; attribute is per function
     const size_t smem = smem_bytes<D>();
@@ -453,7 +467,7 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
         }
         configured = true;
     }
-    attn_fwd_kernel<D><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, p);
+    attn_fwd_kernel<D><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
@@ -490,8 +504,9 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         }
         return 0;
     }
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_tma_bf16_3d(tq, Q, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
+        !make_tma_bf16_3d(to, O, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
         !make_tma_bf16_3d(tk, K, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err) ||
         !make_tma_bf16_3d(tv, V, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err))
         return 5;
@@ -515,8 +530,8 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         err = "attn_fwd: problem too large for one launch";
         return 2;
     }
-    if (d == 128) return launch<128>(tq, tk, tv, p, static_cast<int>(grid), env, err);
-    return launch<64>(tq, tk, tv, p, static_cast<int>(grid), env, err);
+    if (d == 128) return launch<128>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    return launch<64>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
 }
 
 }  // namespace gbattn
