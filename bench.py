@@ -126,7 +126,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -262,6 +262,38 @@ def run_reference(args, rank, world):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
+    """Kernel-only TFLOP/s of the other prefill workloads (inputs resident,
+    L2 flushed before each timed launch, CUDA events around the launch)."""
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, c in wl.WORKLOADS.items():
+        if not isinstance(c, wl.PrefillCase) or name == skip or c.N_q < 1024:
+            continue
+        Q, K, V = (x.to(dev) for x in wl.prefill_inputs(c))
+        O = torch.empty_like(Q)
+        L = torch.empty(c.B, c.H, c.N_q, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            gb.attn_fwd(Q, K, V, causal=c.causal, window=c.window, scale=c.softmax_scale(), O=O, LSE=L)
+        total = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gb.attn_fwd(Q, K, V, causal=c.causal, window=c.window, scale=c.softmax_scale(), O=O, LSE=L)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1) / 1e3
+        gb.check()
+        t = total / reps
+        tf = prefill_flops(c) / t / 1e12
+        gbs = prefill_bytes(c) / t / 1e9
+        out[name] = {"tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"], "ms": t * 1e3,
+                     "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"]}
+        del Q, K, V, O, L
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -409,6 +441,8 @@ def run_ours(args, rank, world, local):
         "wall_s_timed_region": wall,
         "kernel_source": {"attn_fwd": src_p, "mla_decode": src_d},
     }
+    if not args.no_extra:
+        line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)
@@ -446,7 +480,7 @@ def run_profile_case(args, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=PREFILL, choices=[k for k, v in wl.WORKLOADS.items()
@@ -455,6 +489,7 @@ def main():
                                                                   if isinstance(v, wl.MlaCase)])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
                     help="only launch the selected kernel warmup+steps times (for ncu captures)")
     args = ap.parse_args()
