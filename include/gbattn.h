@@ -161,6 +161,17 @@ const char *gbattn_last_error(void);
 uint64_t gbattn_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * gbattn_set_fault_injection -- test hook for the bounded waits (default 0 =
+ * off).  Mode 1: in later attn_fwd launches the TMA producer never loads the
+ * Q tiles, so the tensor-core warp's wait for them runs out after the wait
+ * limit (gbattn_set_wait_timeout_ns); every CTA then stops, frees its tensor
+ * memory and exits, and gbattn_check() returns GBATTN_ERR_TIMEOUT.  Nothing
+ * faults or traps; the CUDA context stays usable.  Not part of the attention
+ * computation (the pages have no counterpart).  Returns the previous mode.
+ */
+int gbattn_set_fault_injection(int mode);
+
+/*
  * gbattn_selftest_umma -- layout check of the tensor-core building blocks the
  * kernels are made of, on one 128x128x128 bf16 tile:
  *   S = A B^T   (A, B: TMA-loaded, 128-byte-swizzled, K-major shared-memory operands)

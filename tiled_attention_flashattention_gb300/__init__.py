@@ -17,7 +17,7 @@ import threading
 import torch
 
 __all__ = ["attn_fwd", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_noalloc", "check", "selftest_umma",
-           "set_wait_timeout_ns", "GbattnError", "library_path", "load_library"]
+           "set_wait_timeout_ns", "set_fault_injection", "GbattnError", "library_path", "load_library"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgbattn.so")
@@ -63,6 +63,8 @@ def load_library():
         lib.gbattn_last_error.restype = ctypes.c_char_p
         lib.gbattn_set_wait_timeout_ns.argtypes = [U64]
         lib.gbattn_set_wait_timeout_ns.restype = U64
+        lib.gbattn_set_fault_injection.argtypes = [I]
+        lib.gbattn_set_fault_injection.restype = I
         lib.gbattn_selftest_umma.argtypes = [P, P, P, P, P, P, P]
         lib.gbattn_selftest_umma.restype = I
         _lib = lib
@@ -206,6 +208,11 @@ def check(stream=None):
 
 def set_wait_timeout_ns(ns: int) -> int:
     return int(load_library().gbattn_set_wait_timeout_ns(int(ns)))
+
+
+def set_fault_injection(mode: int) -> int:
+    """Test hook: 1 makes later attn_fwd launches time out on purpose (see gbattn.h)."""
+    return int(load_library().gbattn_set_fault_injection(int(mode)))
 
 
 def selftest_umma(A, B, P, V, stream=None):

@@ -15,6 +15,7 @@ namespace {
 
 thread_local std::string g_err;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_inject{0};
 
 // Device status word: kernels record the first failed bounded wait here.
 __device__ int g_status_word;
@@ -61,6 +62,7 @@ int get_env(LaunchEnv &env, void *stream)
     env.status = d.status;
     env.timeout_ns = g_timeout_ns.load();
     env.num_sms = d.num_sms;
+    env.inject = g_inject.load();
     return GBATTN_OK;
 }
 
@@ -251,6 +253,12 @@ extern "C" uint64_t gbattn_set_wait_timeout_ns(uint64_t ns)
     if (ns < 1000000ull) ns = 1000000ull;
     if (ns > 60000000000ull) ns = 60000000000ull;
     return g_timeout_ns.exchange(ns);
+}
+
+extern "C" int gbattn_set_fault_injection(int mode)
+{
+    if (mode < 0 || mode > 1) mode = 0;
+    return g_inject.exchange(mode);
 }
 
 extern "C" int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,

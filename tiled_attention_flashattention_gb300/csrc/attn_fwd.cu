@@ -88,6 +88,7 @@ struct Params {
     int group;          // H / H_kv
     int n_qblk;         // ceil(N_q / 256)
     float c;            // scale * log2(e)
+    int inject;         // 1: the producer never loads the Q tiles (tests the bounded waits)
     int *status;
     uint64_t timeout_ns;
 };
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t qbytes = 0;
             for (int t = 0; t < 2; ++t)
                 if (has[t]) qbytes += C::kTileBytes;
+            if (p.inject == 1) qbytes = 0;   // nothing ever completes q_full
             if (qbytes) {
                 mbar_arrive_expect_tx(&c.q_full, qbytes);
                 for (int t = 0; t < 2; ++t)
@@ -523,6 +525,7 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
     p.group = H / H_kv;
     p.n_qblk = (N_q + kQTiles * kBM - 1) / (kQTiles * kBM);
     p.c = scale * 1.4426950408889634f;
+    p.inject = env.inject;
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
     const long long grid = static_cast<long long>(p.n_qblk) * B * H;

@@ -16,6 +16,7 @@ struct LaunchEnv {
     int *status;          // device status word of the current device
     uint64_t timeout_ns;  // limit of every device-side wait
     int num_sms;          // SM count of the current device
+    int inject;           // failure-injection mode for tests (0 = off)
 };
 
 // Prefill attention forward (attn_fwd).  Pointers are device pointers, already
