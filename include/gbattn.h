@@ -124,7 +124,7 @@ int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, cons
  * the same computation as mla_decode, with the same arguments minus the
  * workspace, and allocates nothing: no cudaMalloc, no cudaFree, no allocating
  * library routine.  The split-KV partial results go to a scratch array built
- * into the library instead: 42,024,960 bytes, enough for every shape on GPUs
+ * into the library instead: 21,053,440 bytes, enough for every shape on GPUs
  * with up to 160 SMs, held by every GPU that loads the library until the
  * process exits.  If the current device would need more scratch than that,
  * the call returns GBATTN_ERR_WORKSPACE and enqueues nothing.

@@ -17,32 +17,39 @@
 //   CTA 1 holds latent dims [256, 512) plus the 64 RoPE dims, computes the
 //         partial score over those 320 dims and owns O[:, 256:512).
 // Every KV byte is read from HBM by exactly one CTA.  The two fp32 partial
-// score tiles (128 heads x 64 keys, 32 KB) are swapped with one bulk copy per
-// CTA per tile (TMA engine, shared memory to the peer's shared memory), so
-// both CTAs hold the same full score tile and run the same online softmax;
-// each then multiplies P by its own latent half (V = KV_latent).
+// score tiles are swapped in 32-key units (128 heads x 32 keys, 16 KB) with
+// one bulk copy per CTA per unit (TMA engine, shared memory to the peer's
+// shared memory), so both CTAs hold the same full scores and run the same
+// online softmax; each then multiplies P by its own latent half
+// (V = KV_latent).  Send and receive buffers, and P in TMEM, are
+// double-buffered, so the copy of one unit overlaps the softmax of the other
+// and the tensor cores never wait for the exchange round trip.
 //
 // Work split: the B * ceil(N_kv / 64) key tiles are cut into one contiguous
 // range per cluster (as many clusters as fit on the GPU at once).  A range
 // that covers a whole sequence writes the final O and LSE; a partial range
-// writes O / l and its LSE to the workspace, and a small combine kernel merges
-// the pieces of each split sequence with the exact log-sum-exp rule
-// (TileLang 学习笔记, "Online Softmax 的关键", applied across key ranges).
-// Only the first and the last sequence of a cluster's range can be partial,
-// so the workspace holds two slots per cluster whatever B and N_kv are.
+// writes O / l (bf16) and its LSE to the workspace, and a small combine
+// kernel, launched as a programmatic dependent of the split kernel so that
+// its blocks are already resident when the split kernel ends, merges the
+// pieces of each split sequence with the exact log-sum-exp rule (TileLang
+// 学习笔记, "Online Softmax 的关键", applied across key ranges).  Only the
+// first and the last sequence of a cluster's range can be partial, so the
+// workspace holds two slots per cluster whatever B and N_kv are.
 //
 // Per CTA (384 threads, one CTA per SM):
-//   warp 0      TMA producer: this CTA's dims of each 64-key tile, 4 stages;
-//   warp 1      tcgen05 issuer: S_part = Q_part K_part^T with Q from TMEM,
-//               then O_half += P V_half with P from TMEM (N = 256);
-//   warps 4-7   exchange (one thread per head): this sequence's Q part into
-//               TMEM; per tile read S_part, send it to the peer, add the
-//               peer's part, hand the full score row to the softmax warps;
-//   warps 8-11  softmax (one thread per head): online softmax, P (bf16) into
-//               TMEM, O rescaling, epilogue.
-// The exchange of tile j+1 overlaps the softmax of tile j; the score buffer
-// is released as soon as the exchange warps have read it.
-// TMEM: O half [0, 256), S [256, 320), P [320, 352), Q part [352, 512).
+//   warp 0      TMA producer: through one ring of 4 stages, each range's query
+//               part (two slots) and then this CTA's dims of its 64-key tiles;
+//   warp 1      tcgen05 issuer: S_part = Q_part K_part^T per tile (Q from
+//               TMEM, N = 64) and O_half += P V_half per unit (P from TMEM,
+//               N = 256), each issued as soon as its inputs are ready;
+//   warps 4-7   sender (one thread per head): each range's Q part from the
+//               ring into TMEM (the next range's as soon as the last S of the
+//               current one is read); per tile read S_part and, per unit,
+//               write it to a send buffer and copy that to the peer;
+//   warps 8-11  softmax (one thread per head): own + peer partial scores,
+//               online softmax, P (bf16) into TMEM, O rescaling, epilogue.
+// TMEM: O half [0, 256), S [256, 320), P [320, 352) (two 16-column units),
+// Q part [352, 512).
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -54,7 +61,8 @@ namespace gbattn {
 namespace {
 
 constexpr int kH = 128;                   // heads per tile (MMA M)
-constexpr int kBN = 64;                   // keys per tile
+constexpr int kBN = 64;                   // keys per tile (TMA stage, S MMA N)
+constexpr int kBU = 32;                   // keys per unit (exchange, softmax, PV)
 constexpr int kDc = 512;
 constexpr int kHalf = 256;                // latent dims owned by one CTA
 constexpr int kKvChunk = kBN * 128;       // [64 keys x 64 dims] bf16, one TMA box
@@ -67,8 +75,9 @@ constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColP = 320;
 constexpr uint32_t kColQ = 352;
-constexpr int kXBytes = kH * kBN * 4;     // one partial score tile (fp32)
-constexpr uint32_t kBarX = 1, kBarS = 2;  // named barriers of the exchange / softmax warps
+constexpr int kXBytes = kH * kBU * 4;     // one unit of partial scores (fp32, 128-byte rows)
+constexpr int kQChunk = kH * 128;         // [128 heads x 64 dims] bf16, one TMA box of Q_nope
+constexpr uint32_t kBarX = 1, kBarS = 2;  // named barriers of the sender / softmax warps
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -76,8 +85,9 @@ struct Ctl {
     uint64_t q_full, q_empty;
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full, s_free;
-    uint64_t xfull, xfree, sready;
-    uint64_t p_full, pfree;
+    uint64_t sent[2], own_free[2];      // this CTA's partial of a unit: written / read by the softmax
+    uint64_t xfull[2], xfree[2];        // the peer's partial of a unit: arrived / read (remote arrive)
+    uint64_t p_full[2], pfree[2];       // P unit buffer: written / read by its MMA
     uint64_t o_empty;
     uint64_t drain;
     uint32_t tmem_base;
@@ -85,14 +95,13 @@ struct Ctl {
 };
 
 constexpr size_t kSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + 2 * static_cast<size_t>(kXBytes) + sizeof(Ctl);
+    1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * static_cast<size_t>(kXBytes) + sizeof(Ctl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Params {
-    const __nv_bfloat16 *Qn;   // [B][128][512]
-    const __nv_bfloat16 *Qp;   // [B][128][64]
     __nv_bfloat16 *O;
     float *LSE;
-    float *ws_O;        // [slots][128][512] fp32, O / l of partial ranges
+    __nv_bfloat16 *ws_O;   // [slots][128][512] bf16, O / l of partial ranges
     float *ws_LSE;      // [slots][128]
     int B, N_kv, ntile;
     long long T;        // B * ntile
@@ -115,17 +124,32 @@ __host__ __device__ __forceinline__ int cluster_of_tile(long long x, long long T
     return static_cast<int>(((x + 1) * C - 1) / T);
 }
 
+__device__ __forceinline__ void bulk_wait_read_allow1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// S_part = Q_part K_part^T over NK 16-dim steps: A = Q from TMEM (8 columns
+// per step), B = the stage's 64-dim chunks (K-major, 32 bytes per step).
+template <int NK>
+__device__ __forceinline__ void issue_s(uint32_t d, uint32_t a, uint64_t kvd, uint32_t idesc)
+{
+#pragma unroll
+    for (int k = 0; k < NK; ++k)
+        umma_ts(d, a + k * 8, desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idesc, k > 0 ? 1u : 0u);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
-                     const Params p)
+                     const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *sKV = smem;                                   // [stage][chunk][64 keys][128 B]
-    uint8_t *sSend = sKV + kStages * kStageBytes;          // [128 rows][256 B] fp32, swizzled
-    uint8_t *sRecv = sSend + kXBytes;                      // [128 rows][256 B] fp32, swizzled
-    Ctl &c = *reinterpret_cast<Ctl *>(sRecv + kXBytes);
+    uint8_t *sSend = sKV + kStages * kStageBytes;          // [2][128 rows][128 B] fp32, swizzled
+    uint8_t *sRecv = sSend + 2 * kXBytes;                  // [2][128 rows][128 B] fp32, swizzled
+    Ctl &c = *reinterpret_cast<Ctl *>(sRecv + 2 * kXBytes);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
@@ -145,11 +169,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(&c.s_full, 1);
         mbar_init(&c.s_free, 128);
-        mbar_init(&c.xfull, 1);       // this CTA's expect_tx arrive + the peer's 32 KB
-        mbar_init(&c.xfree, 1);       // remote arrive: the peer's receive buffer is free
-        mbar_init(&c.sready, 128);
-        mbar_init(&c.p_full, 128);
-        mbar_init(&c.pfree, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&c.sent[i], 1);
+            mbar_init(&c.own_free[i], 1);
+            mbar_init(&c.xfull[i], 1);    // this CTA's expect_tx arrive + the peer's 16 KB
+            mbar_init(&c.xfree[i], 1);    // remote arrive: the peer's receive buffer i is free
+            mbar_init(&c.p_full[i], 128);
+            mbar_init(&c.pfree[i], 1);
+        }
         mbar_init(&c.o_empty, 128);
         mbar_init(&c.drain, 1);
         c.abort = 0;
@@ -165,19 +192,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tbase = c.tmem_base;
     const WaitCtl ctl{&c.abort, p.status, p.timeout_ns};
+    // The combine kernel may be scheduled as soon as SMs free up; it waits for
+    // this grid's completion before reading anything.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // =================== TMA producer ===================
         if (lane == 0) {
             tma_prefetch_desc(&tmKV);
             tma_prefetch_desc(&tmKp);
+            tma_prefetch_desc(&tmQn);
+            tma_prefetch_desc(&tmQp);
             bool ok = true;
             int it = 0;
             const uint32_t kvbytes = nch * kKvChunk;
+            const uint32_t qbytes = rank == 0 ? 2 * kQChunk : 2 * kQChunk + kQChunk / 2;
             for (int b = b_first; b <= b_last && ok; ++b) {
                 const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
                 const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
-                for (long long x = x0; x < x1; ++x) {
+                // This sequence's query part: two ring slots, each [128 heads x 64 dims]
+                // chunks 2i and 2i + 1 of Q_nope, plus heads [64i, 64i + 64) of Q_pe on CTA 1.
+                for (int qi = 0; qi < 2; ++qi) {
+                    const int s = it % kStages;
+                    const uint32_t round = static_cast<uint32_t>(it / kStages);
+                    if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
+                    uint8_t *dst = sKV + s * kStageBytes;
+                    mbar_arrive_expect_tx(&c.full[s], qbytes);
+                    tma_load_3d(dst, &tmQn, &c.full[s], dim0 + 2 * qi * 64, 0, b);
+                    tma_load_3d(dst + kQChunk, &tmQn, &c.full[s], dim0 + (2 * qi + 1) * 64, 0, b);
+                    if (rank == 1) tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], 0, qi * 64, b);
+                    ++it;
+                }
+                for (long long x = x0; x < x1 && ok; ++x) {
+                    if (x == max(x0, x1 - 4) && b < b_last) {
+                        // The next range's query and first key tiles into L2 a few tiles
+                        // ahead: its two query slots take half the ring, so its first
+                        // tile is loaded late and must not also pay the HBM latency.
+                        for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmQn, dim0 + ch * 64, 0, b + 1);
+                        if (rank == 1) {
+                            tma_prefetch_l2_3d(&tmQp, 0, 0, b + 1);
+                            tma_prefetch_l2_3d(&tmQp, 0, 64, b + 1);
+                        }
+                        const int nn = static_cast<int>(min(static_cast<long long>(p.ntile), t_end - x1));
+                        for (int j = 0; j < min(nn, 3); ++j) {
+                            for (int ch = 0; ch < 4; ++ch)
+                                tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, j * kBN, b + 1);
+                            if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, j * kBN, b + 1);
+                        }
+                    }
                     const int key0 = static_cast<int>(x - static_cast<long long>(b) * p.ntile) * kBN;
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
@@ -203,50 +265,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32(kH, kBN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kH, kHalf, false, true);
             const uint32_t sKVa = smem_u32(sKV);
-            bool ok = true;
-            int it = 0, seg = 0;
-            uint32_t g = 0;      // global tile counter
-            // O_half += P V_half for tile gp: P from TMEM (8 columns per 16
-            // keys); V = the latent chunks of stage sp read N-major (64-dim
-            // blocks 8 KB apart, 16 keys = 2 KB per MMA).
-            auto issue_pv = [&](uint32_t gp, int sp, bool first) -> bool {
-                if (!mbar_wait(&c.p_full, gp & 1u, ctl)) return false;
-                if (first && seg > 0 && !mbar_wait(&c.o_empty, (seg - 1) & 1, ctl)) return false;
-                tc_fence_after_sync();
-                const uint64_t vd = smem_desc_sw128(sKVa + sp * kStageBytes, kKvChunk, 1024);
-                umma_ts(tbase + kColO, tbase + kColP, vd, idPV, first ? 0u : 1u);
+            const uint32_t aFull = smem_u32(&c.full[0]), aSfree = smem_u32(&c.s_free), aQfull = smem_u32(&c.q_full);
+            const uint32_t aPfull = smem_u32(&c.p_full[0]), aOempty = smem_u32(&c.o_empty);
+            // Two cursors, issued as soon as their inputs are ready: S per
+            // tile and PV per unit, so that S of the next tiles never waits
+            // behind the softmax of an earlier unit.  Readiness is polled
+            // without suspending the thread.
+            const int total = static_cast<int>(t_end - t_begin);
+            const long long bnd0 = (t_begin / p.ntile + 1) * p.ntile;   // first segment boundary
+            // Ring slots: each range of the cluster starts with two query slots,
+            // then one slot per key tile.
+            // S cursor: tile gs (flat t_begin + gs), its ring slot and segment.
+            int gs = 0, s_slot = 2, s_seg = 0;
+            long long s_x = t_begin, s_bnd = bnd0;
+            bool s_first = true;
+            // PV cursor: unit gu of tile gu / 2.
+            int gu = 0, u_slot = 2, u_seg = 0;
+            long long u_x = t_begin, u_bnd = bnd0;
+            bool u_first = true;
+            uint64_t t_last = global_timer_ns();
+            for (uint32_t spin = 1; gu < 2 * total; ++spin) {
+                bool progressed = false;
+                if (gu < 2 * gs) {
+                    // O_half += P V_half for one unit: P from TMEM (8 columns per 16
+                    // keys); V = the latent chunks of the tile's stage read N-major
+                    // (64-dim blocks 8 KB apart, 16 keys = 2 KB per MMA).
+                    const int h = gu & 1;
+                    const uint32_t t = static_cast<uint32_t>(gu >> 1);
+                    const bool first = h == 0 && u_first;
+                    const int u_stage = u_slot % kStages;
+                    if (mbar_poll(aPfull + h * 8, t & 1u) &&
+                        (!first || u_seg == 0 || mbar_poll(aOempty, static_cast<uint32_t>(u_seg - 1) & 1u))) {
+                        tc_fence_after_sync();
+                        const uint64_t vd =
+                            smem_desc_sw128(sKVa + u_stage * kStageBytes + h * (kBU * 128), kKvChunk, 1024);
+                        const uint32_t tp = tbase + kColP + h * (kBU / 2);
+                        umma_ts(tbase + kColO, tp, vd, idPV, first ? 0u : 1u);
 #pragma unroll
-                for (int k = 1; k < kBN / 16; ++k)
-                    umma_ts(tbase + kColO, tbase + kColP + k * 8, desc_advance(vd, k * 2048), idPV, 1u);
-                umma_commit(&c.pfree);
-                umma_commit(&c.empty[sp]);
-                return true;
-            };
-            for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
-                const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
-                const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
-                const int n = static_cast<int>(x1 - x0);
-                if (!(ok = mbar_wait(&c.q_full, seg & 1, ctl))) break;
-                int prev_stage = -1;
-                for (int i = 0; i < n; ++i) {
-                    const int s = it % kStages;
-                    if (!(ok = mbar_wait(&c.full[s], static_cast<uint32_t>(it / kStages) & 1u, ctl))) break;
-                    if (g > 0 && !(ok = mbar_wait(&c.s_free, (g - 1) & 1u, ctl))) break;
-                    tc_fence_after_sync();
-                    // S_part = Q_part K_part^T: Q from TMEM (8 columns per 16 dims).
-                    const uint64_t kvd = smem_desc_sw128(sKVa + s * kStageBytes, 16, 1024);
-                    umma_ts(tbase + kColS, tbase + kColQ, kvd, idS, 0u);
-                    for (int k = 1; k < nch * 4; ++k)
-                        umma_ts(tbase + kColS, tbase + kColQ + k * 8,
-                                desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idS, 1u);
-                    umma_commit(&c.s_full);
-                    if (i == n - 1) umma_commit(&c.q_empty);
-                    if (i > 0 && !(ok = issue_pv(g - 1, prev_stage, i == 1))) break;
-                    prev_stage = s;
-                    ++it;
-                    ++g;
+                        for (int k = 1; k < kBU / 16; ++k)
+                            umma_ts(tbase + kColO, tp + k * 8, desc_advance(vd, k * 2048), idPV, 1u);
+                        umma_commit(&c.pfree[h]);
+                        if (h == 1) {
+                            umma_commit(&c.empty[u_stage]);
+                            ++u_slot;
+                            if (++u_x == u_bnd) {
+                                u_slot += 2;
+                                u_bnd += p.ntile;
+                                ++u_seg;
+                                u_first = true;
+                            } else {
+                                u_first = false;
+                            }
+                        }
+                        ++gu;
+                        progressed = true;
+                    }
                 }
-                if (ok && n > 0) ok = issue_pv(g - 1, prev_stage, n == 1);
+                if (gs < total) {
+                    const int s_stage = s_slot % kStages;
+                    const uint32_t s_phase = static_cast<uint32_t>(s_slot / kStages) & 1u;
+                    if (mbar_poll(aFull + s_stage * 8, s_phase) &&
+                        (gs == 0 || mbar_poll(aSfree, static_cast<uint32_t>(gs - 1) & 1u)) &&
+                        (!s_first || mbar_poll(aQfull, static_cast<uint32_t>(s_seg) & 1u))) {
+                        tc_fence_after_sync();
+                        // S_part = Q_part K_part^T: Q from TMEM (8 columns per 16 dims).
+                        const uint64_t kvd = smem_desc_sw128(sKVa + s_stage * kStageBytes, 16, 1024);
+                        if (rank == 0)
+                            issue_s<16>(tbase + kColS, tbase + kColQ, kvd, idS);
+                        else
+                            issue_s<20>(tbase + kColS, tbase + kColQ, kvd, idS);
+                        umma_commit(&c.s_full);
+                        ++gs;
+                        ++s_x;
+                        if (s_x == s_bnd || gs == total) umma_commit(&c.q_empty);   // last tile of a range
+                        ++s_slot;
+                        if (s_x == s_bnd) {
+                            s_slot += 2;
+                            s_bnd += p.ntile;
+                            ++s_seg;
+                            s_first = true;
+                        } else {
+                            s_first = false;
+                        }
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    spin = 0;
+                    t_last = global_timer_ns();
+                } else if ((spin & 15u) == 0) {
+                    if (*ctl.abort) break;
+                    if (global_timer_ns() - t_last > p.timeout_ns) {
+                        raise_abort(ctl, kStatusWaitTimeout);
+                        break;
+                    }
+                }
             }
             umma_commit(&c.drain);
             volatile int no_abort = 0;
@@ -254,92 +367,111 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait(&c.drain, 0, drain);
         }
     } else if (warp >= 4 && warp < 8) {
-        // =================== Q load + partial-score exchange (one thread per head) ===================
+        // =================== Q load + sender (one thread per head) ===================
         const int quad = warp - 4;
         const int row = quad * 32 + lane;
         const bool leader = threadIdx.x == 128;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t swz = static_cast<uint32_t>(row & 15);
-        const uint32_t peer_recv = mapa_shared(smem_u32(sRecv), peer);
-        const uint32_t peer_xfull = mapa_shared(smem_u32(&c.xfull), peer);
-        float4 *send_row = reinterpret_cast<float4 *>(sSend + row * 256);
-        float4 *recv_row = reinterpret_cast<float4 *>(sRecv + row * 256);
-        bool ok = true;
-        uint32_t g = 0;
+        const uint32_t swz = static_cast<uint32_t>(row & 7);
+        const uint32_t peer_recv[2] = {mapa_shared(smem_u32(sRecv), peer),
+                                       mapa_shared(smem_u32(sRecv + kXBytes), peer)};
+        const uint32_t peer_xfull[2] = {mapa_shared(smem_u32(&c.xfull[0]), peer),
+                                        mapa_shared(smem_u32(&c.xfull[1]), peer)};
+        // This CTA's part of the query rows of a range into TMEM (two bf16 per
+        // column), from the range's two query slots of the ring (128-byte
+        // swizzled rows); slot0 is the ring slot of the first.
+        auto load_q = [&](int slot0) -> bool {
+            for (int qi = 0; qi < 2; ++qi) {
+                const int sl = slot0 + qi, st = sl % kStages;
+                if (!barrier_and(kBarX, 128, mbar_wait(&c.full[st], static_cast<uint32_t>(sl / kStages) & 1u, ctl)))
+                    return false;
+                const uint8_t *src = sKV + st * kStageBytes;
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 *rowp = reinterpret_cast<const uint4 *>(src + j * kQChunk + row * 128);
+                    uint32_t r[32];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 v = rowp[k ^ swz];
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st_x32(tbase + lane_base + kColQ + (2 * qi + j) * 32, r);
+                }
+                if (rank == 1 && (row >> 6) == qi) {   // warp-uniform: heads [64 qi, 64 qi + 64) of Q_pe
+                    const uint4 *rowp = reinterpret_cast<const uint4 *>(src + 2 * kQChunk + (row & 63) * 128);
+                    uint32_t r[32];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 v = rowp[k ^ swz];
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st_x32(tbase + lane_base + kColQ + 128, r);
+                }
+                named_barrier(kBarX, 128);          // every row read: the slot goes back to the producer
+                if (leader) mbar_arrive(&c.empty[st]);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&c.q_full);
+            return true;
+        };
+        bool ok = load_q(0);
+        uint32_t t = 0;          // tiles of this CTA so far
         int seg = 0;
         for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
             const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
             const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
             const int n = static_cast<int>(x1 - x0);
-            // This CTA's part of the query row into TMEM (two bf16 per column).
-            if (seg > 0 && !(ok = barrier_and(kBarX, 128, mbar_wait(&c.q_empty, (seg - 1) & 1, ctl)))) break;
-            const uint4 *qn = reinterpret_cast<const uint4 *>(p.Qn + (static_cast<size_t>(b) * kH + row) * kDc + dim0);
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t r[32];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 v = __ldg(qn + ch * 8 + k);
-                    r[4 * k] = v.x;
-                    r[4 * k + 1] = v.y;
-                    r[4 * k + 2] = v.z;
-                    r[4 * k + 3] = v.w;
-                }
-                tmem_st_x32(tbase + lane_base + kColQ + ch * 32, r);
-            }
-            if (rank == 1) {
-                const uint4 *qp = reinterpret_cast<const uint4 *>(p.Qp + (static_cast<size_t>(b) * kH + row) * 64);
-                uint32_t r[32];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 v = __ldg(qp + k);
-                    r[4 * k] = v.x;
-                    r[4 * k + 1] = v.y;
-                    r[4 * k + 2] = v.z;
-                    r[4 * k + 3] = v.w;
-                }
-                tmem_st_x32(tbase + lane_base + kColQ + 128, r);
-            }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&c.q_full);
-
-            for (int i = 0; i < n; ++i, ++g) {
-                if (!(ok = barrier_and(kBarX, 128, mbar_wait(&c.s_full, g & 1u, ctl)))) break;
+            for (int i = 0; i < n && ok; ++i, ++t) {
+                if (!(ok = barrier_and(kBarX, 128, mbar_wait(&c.s_full, t & 1u, ctl)))) break;
                 tc_fence_after_sync();
-                uint32_t sr[64];
+                uint32_t sr[kBN];
                 tmem_ld_x64(tbase + lane_base + kColS, sr);
                 tc_fence_before_sync();
                 mbar_arrive(&c.s_free);
-                // The previous copy must have finished reading the send buffer.
-                if (leader && g > 0) bulk_wait_read_all();
-                named_barrier(kBarX, 128);
+                if (i == n - 1 && b < b_last) {
+                    // The range's last S is done, and with it every read of its query:
+                    // load the next range's query now, so that its first S does not
+                    // wait for this tile's sends.
+                    if (!(ok = barrier_and(kBarX, 128, mbar_wait(&c.q_empty, seg & 1, ctl)) &&
+                               load_q(2 * (seg + 1) + static_cast<int>(t) + 1)))
+                        break;
+                }
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    send_row[q ^ swz] = make_float4(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1]),
-                                                    __uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3]));
-                fence_proxy_async_smem();      // the copy engine reads the send buffer
-                named_barrier(kBarX, 128);
-                if (leader) {
-                    // The peer's receive buffer is free once its softmax warps read tile g - 1.
-                    bool got = (g == 0) || mbar_wait_cluster(&c.xfree, (g - 1) & 1u, ctl);
-                    if (got) {
-                        mbar_arrive_expect_tx(&c.xfull, kXBytes);   // this CTA's incoming tile
-                        bulk_copy_to_peer(peer_recv, sSend, kXBytes, peer_xfull);
-                        bulk_commit_group();
+                for (int h = 0; h < 2; ++h) {
+                    // Send buffer h was last read by the copy of unit (t - 1, h)
+                    // (at most the other buffer's copy may still be pending) and
+                    // by this CTA's softmax.
+                    bool got = true;
+                    if (leader && t > 0) {
+                        bulk_wait_read_allow1();
+                        got = mbar_wait(&c.own_free[h], (t - 1) & 1u, ctl);
+                    }
+                    if (!(ok = barrier_and(kBarX, 128, got))) break;
+                    float4 *srow = reinterpret_cast<float4 *>(sSend + h * kXBytes + row * 128);
+#pragma unroll
+                    for (int q = 0; q < kBU / 4; ++q)
+                        srow[q ^ swz] = make_float4(
+                            __uint_as_float(sr[h * kBU + 4 * q]), __uint_as_float(sr[h * kBU + 4 * q + 1]),
+                            __uint_as_float(sr[h * kBU + 4 * q + 2]), __uint_as_float(sr[h * kBU + 4 * q + 3]));
+                    fence_proxy_async_smem();      // the copy engine reads the send buffer
+                    named_barrier(kBarX, 128);
+                    if (leader) {
+                        // The peer's receive buffer h is free once its softmax read unit (t - 1, h).
+                        if (t == 0 || mbar_wait(&c.xfree[h], (t - 1) & 1u, ctl)) {
+                            mbar_arrive_expect_tx(&c.xfull[h], kXBytes);   // the peer's unit (t, h)
+                            bulk_copy_to_peer(peer_recv[h], sSend + h * kXBytes, kXBytes, peer_xfull[h]);
+                            bulk_commit_group();
+                            mbar_arrive(&c.sent[h]);
+                        }
                     }
                 }
-                if (!(ok = barrier_and(kBarX, 128, mbar_wait_cluster(&c.xfull, g & 1u, ctl)))) break;
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    float4 v = recv_row[q ^ swz];
-                    v.x += __uint_as_float(sr[4 * q]);
-                    v.y += __uint_as_float(sr[4 * q + 1]);
-                    v.z += __uint_as_float(sr[4 * q + 2]);
-                    v.w += __uint_as_float(sr[4 * q + 3]);
-                    recv_row[q ^ swz] = v;
-                }
-                mbar_arrive(&c.sready);
             }
         }
         if (leader) bulk_wait_all();   // no copy of this CTA may still be writing to the peer
@@ -352,106 +484,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tO = tbase + lane_base + kColO;
         const float cexp = p.c;
         const float thr = kRescaleLog2 / cexp;
-        const uint32_t swz = static_cast<uint32_t>(row & 15);
-        const uint32_t peer_xfree = mapa_shared(smem_u32(&c.xfree), peer);
-        const float4 *recv_row = reinterpret_cast<const float4 *>(sRecv + row * 256);
+        const uint32_t swz = static_cast<uint32_t>(row & 7);
+        const uint32_t peer_xfree[2] = {mapa_shared(smem_u32(&c.xfree[0]), peer),
+                                        mapa_shared(smem_u32(&c.xfree[1]), peer)};
         bool ok = true;
-        uint32_t g = 0;
+        bool okw = true;         // this warp's waits so far (agreed on at the next barrier)
+        uint32_t t = 0;
         int seg = 0;
         for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
             const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
             const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
             const int n = static_cast<int>(x1 - x0);
             float m_ref = -INFINITY, l = 0.f;
-            for (int i = 0; i < n; ++i, ++g) {
-                const bool got = mbar_wait(&c.sready, g & 1u, ctl);
-                float s[64];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 v = recv_row[q ^ swz];
-                    s[4 * q] = v.x;
-                    s[4 * q + 1] = v.y;
-                    s[4 * q + 2] = v.z;
-                    s[4 * q + 3] = v.w;
-                }
-                // all 128 rows read: the peer may send its next tile
-                if (!(ok = barrier_and(kBarS, 128, got))) break;
-                if (leader) mbar_arrive_remote(peer_xfree);
-
-                const int key0 = static_cast<int>(x0 + i - static_cast<long long>(b) * p.ntile) * kBN;
-                if (key0 + kBN > p.N_kv) {
-#pragma unroll
-                    for (int k = 0; k < 64; ++k)
-                        if (key0 + k >= p.N_kv) s[k] = -INFINITY;
-                }
-                float mx = s[0];
-#pragma unroll
-                for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
-                const bool move = mx > m_ref + thr;
-                const float new_ref = move ? mx : m_ref;
-                const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
-                m_ref = new_ref;
-                const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-                float sum = 0.f;
-                uint32_t pk[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
-                    const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
-                    sum += p0 + p1;
-                    pk[k] = pack_bf16x2(p0, p1);
-                }
-                l = l * alpha + sum;
-                // PV of the previous tile must be done: it read the P buffer,
-                // and O must be stable before it is rescaled.
-                if (g > 0 && !(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree, (g - 1) & 1u, ctl)))) break;
-                tc_fence_after_sync();
-                if (i > 0 && __any_sync(0xffffffffu, move)) {
+            for (int i = 0; i < n && ok; ++i, ++t) {
 #pragma unroll 1
-                    for (int ch = 0; ch < kHalf / 32; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld_x32(tO + ch * 32, o);
+                for (int h = 0; h < 2; ++h) {
+                    const bool got = mbar_wait(&c.sent[h], t & 1u, ctl) &&
+                                     mbar_wait(&c.xfull[h], t & 1u, ctl);
+                    float s[kBU];
+                    const float4 *orow = reinterpret_cast<const float4 *>(sSend + h * kXBytes + row * 128);
+                    const float4 *rrow = reinterpret_cast<const float4 *>(sRecv + h * kXBytes + row * 128);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st_x32(tO + ch * 32, o);
+                    for (int q = 0; q < kBU / 4; ++q) {
+                        const float4 u = orow[q ^ swz];
+                        const float4 v = rrow[q ^ swz];
+                        s[4 * q] = u.x + v.x;
+                        s[4 * q + 1] = u.y + v.y;
+                        s[4 * q + 2] = u.z + v.z;
+                        s[4 * q + 3] = u.w + v.w;
                     }
+                    // all 128 rows read: the sender may reuse send buffer h and the
+                    // peer may copy its next unit into receive buffer h
+                    if (!(ok = barrier_and(kBarS, 128, got && okw))) break;
+                    if (leader) {
+                        mbar_arrive(&c.own_free[h]);
+                        mbar_arrive_remote(peer_xfree[h]);
+                    }
+
+                    const int key0 = static_cast<int>(x0 + i - static_cast<long long>(b) * p.ntile) * kBN + h * kBU;
+                    if (key0 + kBU > p.N_kv) {
+#pragma unroll
+                        for (int k = 0; k < kBU; ++k)
+                            if (key0 + k >= p.N_kv) s[k] = -INFINITY;
+                    }
+                    float mx = s[0];
+#pragma unroll
+                    for (int k = 1; k < kBU; ++k) mx = fmaxf(mx, s[k]);
+                    const bool move = mx > m_ref + thr;
+                    const float new_ref = move ? mx : m_ref;
+                    const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
+                    m_ref = new_ref;
+                    const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
+                    float sum = 0.f;
+                    uint32_t pk[kBU / 2];
+#pragma unroll
+                    for (int k = 0; k < kBU / 2; ++k) {
+                        const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
+                        const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
+                        sum += p0 + p1;
+                        pk[k] = pack_bf16x2(p0, p1);
+                    }
+                    l = l * alpha + sum;
+                    // P buffer h was read by the MMA of unit (t - 1, h).
+                    if (t > 0) okw = __all_sync(0xffffffffu, mbar_wait(&c.pfree[h], (t - 1) & 1u, ctl)) && okw;
+                    // O must hold every earlier unit of this range before it is rescaled.
+                    if ((i > 0 || h > 0) && __any_sync(0xffffffffu, move)) {
+                        const bool prev = h == 1 ? mbar_wait(&c.pfree[0], t & 1u, ctl)
+                                                 : mbar_wait(&c.pfree[1], (t - 1) & 1u, ctl);
+                        okw = __all_sync(0xffffffffu, prev) && okw;
+                        tc_fence_after_sync();
+#pragma unroll 1
+                        for (int ch = 0; ch < kHalf / 32; ++ch) {
+                            uint32_t o[32];
+                            tmem_ld_x32(tO + ch * 32, o);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tmem_st_x32(tO + ch * 32, o);
+                        }
+                    }
+                    tc_fence_after_sync();
+                    tmem_st_x16(tbase + lane_base + kColP + h * (kBU / 2), pk);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    mbar_arrive(&c.p_full[h]);
                 }
-                tmem_st_x32(tbase + lane_base + kColP, pk);
-                tmem_st_wait();
-                tc_fence_before_sync();
-                mbar_arrive(&c.p_full);
             }
             if (!ok) break;
 
             // ---- epilogue of this range of sequence b (after its last PV)
-            if (!(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree, (g - 1) & 1u, ctl)))) break;
+            if (!(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree[1], (t - 1) & 1u, ctl) && okw))) break;
             tc_fence_after_sync();
             const bool whole = (n == p.ntile);
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             const float lse = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
             const size_t slot = static_cast<size_t>(cl) * 2 + (b == b_first ? 0 : 1);
+            // O / l of this range, bf16, to the final output (a whole sequence)
+            // or to the workspace slot (a part of a split sequence).
+            __nv_bfloat16 *obase = whole ? p.O + (static_cast<size_t>(b) * kH + row) * kDc + dim0
+                                         : p.ws_O + (slot * kH + row) * kDc + dim0;
 #pragma unroll 1
             for (int ch = 0; ch < kHalf / 32; ++ch) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + ch * 32, o);
-                if (whole) {
-                    uint4 v[4];
-                    uint32_t *w = reinterpret_cast<uint32_t *>(v);
+                uint4 v[4];
+                uint32_t *w = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * kH + row) * kDc +
-                                                           dim0 + ch * 32);
+                for (int k = 0; k < 16; ++k)
+                    w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                uint4 *dst = reinterpret_cast<uint4 *>(obase + ch * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = v[k];
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_O + (slot * kH + row) * kDc + dim0 + ch * 32);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                                             __uint_as_float(o[4 * k + 2]) * inv_l,
-                                             __uint_as_float(o[4 * k + 3]) * inv_l);
-                }
+                for (int k = 0; k < 4; ++k) dst[k] = v[k];
             }
             if (rank == 0) {
                 if (whole)
@@ -477,12 +619,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
-// Merge the partial ranges of each split sequence: LSE = ln sum_s e^{LSE_s},
-// O = sum_s e^{LSE_s - LSE} O_s.  One block per (sequence, group of 16
+// Merge the parts of each split sequence: LSE = ln sum_q e^{LSE_q},
+// O = sum_q e^{LSE_q - LSE} (O_q / l_q).  One block per (sequence, group of 16
 // heads), 256 threads, 32 output dims per thread; sequences written whole by
-// the split kernel are skipped.
+// the split kernel are skipped.  Up to three parts (the usual case) every
+// load of a thread is issued at once.
 __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the split kernel is complete
     const int b = blockIdx.x / 8, hg = blockIdx.x % 8;
     const long long x0 = static_cast<long long>(b) * p.ntile;
     const int c0 = cluster_of_tile(x0, p.T, p.C);
@@ -490,31 +634,61 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     if (c0 == c1) return;
     const int h = hg * 16 + threadIdx.x / 16;
     const int d0 = (threadIdx.x % 16) * 32;
-    float mx = -INFINITY;
-    for (int q = c0; q <= c1; ++q) {
-        const size_t slot = static_cast<size_t>(q) * 2 + (b == range_start(q, p.T, p.C) / p.ntile ? 0 : 1);
-        mx = fmaxf(mx, p.ws_LSE[slot * kH + h]);
-    }
-    float denom = 0.f;
-    for (int q = c0; q <= c1; ++q) {
-        const size_t slot = static_cast<size_t>(q) * 2 + (b == range_start(q, p.T, p.C) / p.ntile ? 0 : 1);
-        denom += expf(p.ws_LSE[slot * kH + h] - mx);
-    }
-    const float lse = mx + logf(denom);
+    auto slot_of = [&](int q) -> size_t {
+        return static_cast<size_t>(q) * 2 + (b == range_start(q, p.T, p.C) / p.ntile ? 0 : 1);
+    };
+    auto accumulate = [](float (&acc)[32], float w, const uint4 (&v)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[8 * k + 2 * j] += w * __uint_as_float(u[j] << 16);
+                acc[8 * k + 2 * j + 1] += w * __uint_as_float(u[j] & 0xffff0000u);
+            }
+        }
+    };
     float acc[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-    for (int q = c0; q <= c1; ++q) {
-        const size_t slot = static_cast<size_t>(q) * 2 + (b == range_start(q, p.T, p.C) / p.ntile ? 0 : 1);
-        const float w = expf(p.ws_LSE[slot * kH + h] - lse);
-        const float4 *src = reinterpret_cast<const float4 *>(p.ws_O + (slot * kH + h) * kDc + d0);
+    float lse;
+    const int n = c1 - c0 + 1;
+    if (n <= 3) {
+        float lq[3];
+        uint4 v[3][4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 v = src[k];
-            acc[4 * k] += w * v.x;
-            acc[4 * k + 1] += w * v.y;
-            acc[4 * k + 2] += w * v.z;
-            acc[4 * k + 3] += w * v.w;
+        for (int i = 0; i < 3; ++i) {
+            lq[i] = -INFINITY;
+            if (i < n) {
+                const size_t sq = slot_of(c0 + i);
+                lq[i] = p.ws_LSE[sq * kH + h];
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.ws_O + (sq * kH + h) * kDc + d0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[i][k] = src[k];
+            }
+        }
+        const float mx = fmaxf(fmaxf(lq[0], lq[1]), lq[2]);
+        float denom = 0.f;
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (i < n) denom += expf(lq[i] - mx);
+        lse = mx + logf(denom);
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (i < n) accumulate(acc, expf(lq[i] - lse), v[i]);
+    } else {
+        float mx = -INFINITY;
+        for (int q = c0; q <= c1; ++q) mx = fmaxf(mx, p.ws_LSE[slot_of(q) * kH + h]);
+        float denom = 0.f;
+        for (int q = c0; q <= c1; ++q) denom += expf(p.ws_LSE[slot_of(q) * kH + h] - mx);
+        lse = mx + logf(denom);
+        for (int q = c0; q <= c1; ++q) {
+            const size_t sq = slot_of(q);
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.ws_O + (sq * kH + h) * kDc + d0);
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = src[k];
+            accumulate(acc, expf(p.ws_LSE[sq * kH + h] - lse), v);
         }
     }
     uint4 out[4];
@@ -574,7 +748,7 @@ Plan make_plan(int B, int N_kv, int clusters)
 
 size_t plan_bytes(const Plan &pl)
 {
-    return pl.slots * kH * kDc * sizeof(float) + pl.slots * kH * sizeof(float);
+    return pl.slots * kH * kDc * sizeof(__nv_bfloat16) + pl.slots * kH * sizeof(float);
 }
 
 // ---------------------------------------------------------------------------
@@ -586,12 +760,12 @@ size_t plan_bytes(const Plan &pl)
 // plain C caller with no allocator of its own.  For them the split-KV partial
 // results live in this fixed array instead of a caller-provided workspace.
 // It is sized for the largest plan this kernel makes on GPUs with up to 160
-// SMs: 80 two-CTA clusters x 2 partial slots x (128 x 512 fp32 O + 128 fp32
-// LSE) = 42,024,960 bytes.  Every GPU that loads the library holds it until
-// the process exits.
+// SMs: 80 two-CTA clusters x 2 partial slots x (128 x 512 bf16 O + 128 fp32
+// LSE) = 21,053,440 bytes.  Every
+// GPU that loads the library holds it until the process exits.
 constexpr size_t kNoAllocMaxClusters = 80;
 constexpr size_t kNoAllocScratchBytes =
-    kNoAllocMaxClusters * 2 * (static_cast<size_t>(kH) * kDc * sizeof(float) + kH * sizeof(float));
+    kNoAllocMaxClusters * 2 * (static_cast<size_t>(kH) * kDc * sizeof(__nv_bfloat16) + kH * sizeof(float));
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 }  // namespace
@@ -657,16 +831,15 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
         err = "mla_decode: workspace too small";
         return 4;
     }
-    CUtensorMap tkv, tkp;
-    if (!make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) || !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err))
+    CUtensorMap tkv, tkp, tqn, tqp;
+    if (!make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) || !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
+        !make_tma_bf16_3d(tqn, Q_nope, d_c, kH, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
         return 5;
     Params p;
-    p.Qn = static_cast<const __nv_bfloat16 *>(Q_nope);
-    p.Qp = static_cast<const __nv_bfloat16 *>(Q_pe);
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-    p.ws_O = static_cast<float *>(workspace);
-    p.ws_LSE = p.ws_O + pl.slots * kH * kDc;
+    p.ws_O = static_cast<__nv_bfloat16 *>(workspace);
+    p.ws_LSE = reinterpret_cast<float *>(p.ws_O + pl.slots * kH * kDc);
     p.B = B;
     p.N_kv = N_kv;
     p.ntile = pl.ntile;
@@ -679,14 +852,22 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     cudaError_t e = cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
-        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, p);
+        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, tqn, tqp, p);
         e = cudaGetLastError();
     }
     bool split = false;   // does a cluster range boundary fall inside a sequence?
     for (int cl = 1; cl < pl.C && !split; ++cl) split = range_start(cl, pl.T, pl.C) % pl.ntile != 0;
     if (e == cudaSuccess && split) {
-        mla_combine_kernel<<<B * 8, 256, 0, env.stream>>>(p);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(B) * 8, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = env.stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
     }
     if (e != cudaSuccess) {
         err = std::string("mla_decode launch: ") + cudaGetErrorString(e);

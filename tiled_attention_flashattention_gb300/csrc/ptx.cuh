@@ -120,6 +120,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar_addr, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity: unlike try_wait it
+// never suspends the thread, so one thread can poll several barriers.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Bounded: returns
 // false (and raises the CTA abort flag) when the limit runs out or another
 // thread already aborted.
@@ -502,6 +516,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Bulk copy (TMA engine) of `bytes` from global memory into this CTA's shared
+// memory, completing the bytes on this CTA's mbarrier `bar`.  Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Bulk copy (TMA engine) of `bytes` bytes from this CTA's shared memory to
 // another CTA's shared memory (dst and bar are shared::cluster addresses from
 // mapa_shared); the bytes complete on that CTA's mbarrier.  Both addresses
@@ -553,43 +578,15 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier shared::cluster writes to it.
+// Arrive on an mbarrier of another CTA of the cluster (default release at CTA
+// scope: the thread's earlier shared-memory reads are complete before the
+// peer can see the arrive).  A cluster-scope release fence here costs about
+// a thousand cycles on the arriving thread and is not needed to hand a
+// buffer back to the peer's copy engine.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr)
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr)
                  : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar_addr, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar_addr), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait with cluster-scope acquire (for phases completed by arrivals
-// from another CTA of the cluster).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const WaitCtl &ctl)
-{
-    const uint32_t a = smem_u32(bar);
-    if (mbar_test_cluster(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test_cluster(a, parity)) return true;
-        if ((it & 15u) == 0) {
-            if (*ctl.abort) return false;
-            if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                raise_abort(ctl, kStatusWaitTimeout);
-                return false;
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
