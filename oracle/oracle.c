@@ -28,7 +28,11 @@
  *  - the mask is additive 0 / -inf: a masked key is excluded entirely;
  *  - causal alignment is bottom-right: key j is allowed for query i iff
  *    j <= i + (N_kv - N_q);
- *  - a window w > 0 (causal only) keeps keys j >= i + (N_kv - N_q) - w + 1;
+ *  - with causal, a window w > 0 keeps keys j >= i + (N_kv - N_q) - w + 1;
+ *  - without causal, a window w > 0 is the symmetric local window of the
+ *    TileLang study notes ("TileLang 学习笔记", section on local attention
+ *    variants: keys from seqpos - w to seqpos + w): with i' = i + (N_kv - N_q),
+ *    key j is visible iff i' - w <= j <= i' + w;
  *  - GQA maps query head h to key/value head h / (H / H_kv) (contiguous
  *    groups; the FlashMLA article's section 5.1 shows only kv_head_num = 1);
  *  - a row with no allowed key has O = 0 and LSE = -inf.
@@ -54,8 +58,12 @@ static double bf16_to_f64(uint16_t bits)
 static int key_allowed(long i, long j, long n_q, long n_kv, int causal, long window)
 {
     long off = n_kv - n_q;
-    if (causal && j > i + off) return 0;
-    if (window > 0 && j < i + off - window + 1) return 0;
+    if (causal) {
+        if (j > i + off) return 0;
+        if (window > 0 && j < i + off - window + 1) return 0;
+    } else if (window > 0) {
+        if (j < i + off - window || j > i + off + window) return 0;
+    }
     return 1;
 }
 
@@ -173,7 +181,6 @@ int oracle_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, dou
                     int window, double scale, const int64_t *rows, int64_t n_rows, int n_threads)
 {
     if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv || N_q < 0 || N_kv < 0 || d <= 0) return -1;
-    if (window > 0 && !causal) return -1;
     int64_t total = (int64_t)B * H * N_q;
     if (!rows) n_rows = total;
     if (n_rows == 0) return 0;

@@ -12,8 +12,10 @@ max subtraction, log base 2 instead of e) fails at least one of them:
   LSE = ln(count);
 * reductions to library routines: torch's fp64 scaled_dot_product_attention,
   torch.logsumexp, repeat_interleave for GQA;
-* structural identities of the masks (window >= N is causal; bottom-right
-  causal rows are the tail rows of the square problem);
+* structural identities of the masks (window >= N is causal, a symmetric
+  window >= N is unmasked; bottom-right causal rows are the tail rows of the
+  square problem); the symmetric window equals torch's fp64 attention with an
+  explicit band mask;
 * an independent fp64 implementation of the online (block-by-block)
   recurrence, and the exact log-sum-exp merge of two key halves.
 """
@@ -65,7 +67,7 @@ def test_single_key_returns_its_value():
     np.testing.assert_allclose(LSE, dots.numpy(), atol=1e-10, rtol=0)
 
 
-@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 3)])
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 3), (False, 2)])
 def test_probability_rows_sum_to_one(causal, window):
     Q, K, V = wl.random_prefill(1, 2, 1, 9, 9, 8, seed=2)
     _, _, P = oracle.attn_fwd(Q, K, V, causal, window, 0.5, return_probs=True)
@@ -76,6 +78,10 @@ def test_probability_rows_sum_to_one(causal, window):
         assert (P[..., j > i] == 0).all()
         if window:
             assert (P[..., j < i - window + 1] == 0).all()
+    elif window:
+        i, j = np.meshgrid(np.arange(9), np.arange(9), indexing="ij")
+        assert (P[..., (j < i - window) | (j > i + window)] == 0).all()
+        assert (P[..., np.abs(j - i) <= window] > 0).all()
 
 
 def test_constant_value_rows_come_back():
@@ -113,7 +119,8 @@ def test_per_row_score_shift():
 
 
 @pytest.mark.parametrize("n_q,n_kv,causal,window", [(8, 8, False, 0), (8, 8, True, 0), (5, 9, True, 0),
-                                                    (9, 9, True, 4), (3, 10, True, 2)])
+                                                    (9, 9, True, 4), (3, 10, True, 2), (9, 9, False, 2),
+                                                    (4, 11, False, 3), (10, 7, False, 4)])
 def test_uniform_scores_closed_form(n_q, n_kv, causal, window):
     _, K, V = wl.random_prefill(1, 1, 1, n_q, n_kv, 8, seed=6)
     Q = torch.zeros(1, 1, n_q, 8, dtype=torch.bfloat16)
@@ -121,8 +128,14 @@ def test_uniform_scores_closed_form(n_q, n_kv, causal, window):
     v = f64(V[0, 0]).numpy()
     off = n_kv - n_q
     for i in range(n_q):
-        hi = min(n_kv - 1, i + off) if causal else n_kv - 1
-        lo = max(0, i + off - window + 1) if window else 0
+        if causal:
+            hi = min(n_kv - 1, i + off)
+            lo = max(0, i + off - window + 1) if window else 0
+        elif window:        # symmetric window: |j - (i + off)| <= window
+            hi = min(n_kv - 1, i + off + window)
+            lo = max(0, i + off - window)
+        else:
+            lo, hi = 0, n_kv - 1
         np.testing.assert_allclose(O[0, 0, i], v[lo:hi + 1].mean(0), atol=1e-12)
         assert abs(LSE[0, 0, i] - math.log(hi - lo + 1)) < 1e-12
 
@@ -161,6 +174,35 @@ def test_window_at_least_n_is_causal():
         Ow, Lw = oracle.attn_fwd(Q, K, V, True, w, 0.3)
         np.testing.assert_array_equal(Oc, Ow)
         np.testing.assert_array_equal(Lc, Lw)
+
+
+def test_symmetric_window_at_least_n_is_unmasked():
+    Q, K, V = wl.random_prefill(1, 2, 2, 13, 13, 8, seed=19)
+    On, Ln = oracle.attn_fwd(Q, K, V, False, 0, 0.3)
+    for w in (12, 30):
+        Ow, Lw = oracle.attn_fwd(Q, K, V, False, w, 0.3)
+        np.testing.assert_array_equal(On, Ow)
+        np.testing.assert_array_equal(Ln, Lw)
+    Ow, _ = oracle.attn_fwd(Q, K, V, False, 11, 0.3)      # row 0 then misses key 12
+    assert not np.array_equal(On, Ow)
+
+
+@pytest.mark.parametrize("n_q,n_kv,w", [(20, 20, 3), (12, 20, 5), (20, 15, 2)])
+def test_symmetric_window_matches_sdpa_with_band_mask(n_q, n_kv, w):
+    Q, K, V = wl.random_prefill(2, 4, 2, n_q, n_kv, 16, seed=20)
+    scale = 0.25
+    O, LSE = oracle.attn_fwd(Q, K, V, False, w, scale)
+    i = torch.arange(n_q)[:, None] + (n_kv - n_q)
+    j = torch.arange(n_kv)[None, :]
+    band = (j >= i - w) & (j <= i + w)
+    Kr, Vr = (f64(x).repeat_interleave(2, dim=1) for x in (K, V))
+    rows = band.any(1)                       # rows with at least one key (the others: O = 0, LSE = -inf)
+    ref = torch.nn.functional.scaled_dot_product_attention(f64(Q), Kr, Vr, attn_mask=band, scale=scale)
+    np.testing.assert_allclose(O[:, :, rows.numpy()], ref[:, :, rows].numpy(), atol=1e-12, rtol=0)
+    s = (f64(Q) @ Kr.transpose(-1, -2)) * scale
+    s = s.masked_fill(~band, -math.inf)
+    np.testing.assert_allclose(LSE, torch.logsumexp(s, -1).numpy(), atol=1e-12, rtol=0)
+    assert (O[:, :, ~rows.numpy()] == 0).all()
 
 
 def test_bottom_right_causal_is_tail_of_square():
@@ -259,8 +301,6 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.attn_fwd(Q, K, V, False, 0, 1.0)
     Q, K, V = wl.random_prefill(1, 2, 2, 4, 4, 8, seed=18)
-    with pytest.raises(ValueError):
-        oracle.attn_fwd(Q, K, V, False, 3, 1.0)                 # window without causal
     with pytest.raises(ValueError):
         oracle.attn_fwd(Q, K, V, False, 0, 1.0, rows=[8])       # row out of range
 
