@@ -49,14 +49,23 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 
 # ---------------------------------------------------------------- workload arithmetic
+def key_bounds(i, N_q: int, N_kv: int, causal: bool, window: int):
+    """Inclusive visible-key bounds (lo, hi) of query rows i (int64 array)."""
+    off = N_kv - N_q
+    if causal:
+        hi = np.minimum(N_kv - 1, i + off)
+        lo = np.maximum(0, i + off - window + 1) if window > 0 else np.zeros_like(i)
+    elif window > 0:        # symmetric local window
+        hi = np.minimum(N_kv - 1, i + off + window)
+        lo = np.maximum(0, i + off - window)
+    else:
+        hi, lo = np.full_like(i, N_kv - 1), np.zeros_like(i)
+    return lo, hi
+
+
 def allowed_pairs(N_q: int, N_kv: int, causal: bool, window: int) -> int:
     """Number of (query, key) pairs the mask keeps, per (batch, head)."""
-    if not causal:
-        return N_q * N_kv
-    i = np.arange(N_q, dtype=np.int64)
-    off = N_kv - N_q
-    hi = np.minimum(N_kv - 1, i + off)
-    lo = np.maximum(0, i + off - window + 1) if window > 0 else np.zeros_like(i)
+    lo, hi = key_bounds(np.arange(N_q, dtype=np.int64), N_q, N_kv, causal, window)
     return int(np.maximum(0, hi - lo + 1).sum())
 
 
@@ -196,10 +205,7 @@ def oracle_sample_rate(case, rows, kind):
         Q, K, V = case["inputs"]
         c = case["case"]
         oracle.attn_fwd(Q, K, V, c.causal, c.window, c.softmax_scale(), rows=rows)
-        i = rows % c.N_q
-        off = c.N_kv - c.N_q
-        hi = np.minimum(c.N_kv - 1, i + off) if c.causal else np.full_like(i, c.N_kv - 1)
-        lo = np.maximum(0, i + off - c.window + 1) if c.window > 0 else np.zeros_like(i)
+        lo, hi = key_bounds(np.asarray(rows, dtype=np.int64) % c.N_q, c.N_q, c.N_kv, c.causal, c.window)
         flops = float((4 * c.d * np.maximum(0, hi - lo + 1)).sum())
     else:
         Qn, Qp, KV, Kp = case["inputs"]

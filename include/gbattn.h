@@ -2,8 +2,8 @@
  * gbattn.h -- C ABI of libgbattn.so: fused attention forward on one GB300
  * (sm_103a), in two forms.
  *
- *  attn_fwd    FlashAttention-style prefill, MHA or GQA, optional causal mask
- *              and causal sliding window.
+ *  attn_fwd    FlashAttention-style prefill, MHA or GQA, optional causal mask,
+ *              causal sliding window and symmetric local window.
  *  mla_decode  FlashMLA-style decode: one query token per sequence, H query
  *              heads sharing one latent KV head (d_c = 512) plus a RoPE key
  *              part (d_r = 64); the values are the latent KV rows themselves.
@@ -66,6 +66,9 @@ typedef enum {
  *   causal = 0, window <= 0 : every key j in [0, N_kv)
  *   causal = 1              : j <= i + off
  *   causal = 1, window > 0  : i + off - window + 1 <= j <= i + off
+ *   causal = 0, window > 0  : i + off - window <= j <= i + off + window
+ *                             (the symmetric local window of the study notes'
+ *                             local-attention variant: seqpos - w .. seqpos + w)
  * A row with no allowed key gets O = 0 and LSE = -inf.
  *
  * Arguments
@@ -74,7 +77,7 @@ typedef enum {
  *   LSE  fp32 [B, H,    N_q]         (written)
  *   d in {64, 128};  B, H, H_kv >= 1;  H % H_kv == 0;  N_q, N_kv >= 0;
  *   scale finite and > 0 (usually 1/sqrt(d));  causal in {0, 1};
- *   window > 0 requires causal = 1 (else GBATTN_ERR_UNSUPPORTED).
+ *   window <= 0 means no window.
  * O and LSE must not overlap the inputs.
  */
 int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,

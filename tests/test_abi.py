@@ -53,7 +53,7 @@ def test_attn_fwd_argument_errors(lib):
     assert _attn(lib, scale=0.0) == 1
     assert _attn(lib, scale=float("nan")) == 1
     assert _attn(lib, d=96) == 2                            # unsupported head dim
-    assert _attn(lib, window=4, causal=0) == 2              # window needs causal
+    assert _attn(lib, window=4, causal=0, Q=0) == 1         # a symmetric window is accepted: the null Q is the error
     assert _attn(lib, Q=0) == 1                             # null pointer
     assert _attn(lib, K=24) == 3                            # misaligned
     assert _attn(lib, LSE=18) == 3

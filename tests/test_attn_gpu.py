@@ -61,6 +61,13 @@ SMALL = [
     (1, 1, 1, 1, 1000, 64, True, 0),
     (3, 8, 8, 130, 1, 128, False, 0),
     (1, 1, 1, 1030, 1030, 128, False, 0),
+    # symmetric local window (causal = 0, window > 0): |j - (i + N_kv - N_q)| <= window
+    (1, 2, 2, 500, 500, 128, False, 64),
+    (1, 2, 1, 333, 333, 64, False, 1),
+    (1, 2, 2, 200, 700, 128, False, 100),   # N_q < N_kv
+    (1, 2, 2, 700, 200, 128, False, 50),    # N_q > N_kv: the first rows see no key
+    (2, 4, 2, 1030, 1030, 128, False, 300),
+    (1, 2, 2, 400, 400, 64, False, 400),    # window >= N: unmasked
 ]
 
 
@@ -132,6 +139,7 @@ def test_workload_mha_causal_2k_full():
 
 @pytest.mark.parametrize("name", ["gqa_causal_b2_h32_hkv8_n8192_d128",
                                   "gqa_window256_b2_h32_hkv8_n8192_d128",
+                                  "gqa_swindow256_b2_h32_hkv8_n8192_d128",
                                   "mha_causal_spiky_b1_h32_n16384_d128"])
 def test_workload_sampled(name):
     _workload_parity(name, 160)

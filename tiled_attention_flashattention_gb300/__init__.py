@@ -104,8 +104,9 @@ def attn_fwd(Q, K, V, causal: bool = False, window: int = 0, scale: float | None
              O=None, LSE=None, stream=None):
     """Fused attention forward.  Q [B,H,N_q,d], K/V [B,H_kv,N_kv,d] bf16 CUDA tensors.
 
-    Returns (O [B,H,N_q,d] bf16, LSE [B,H,N_q] fp32).  ``window > 0`` (causal
-    only) keeps keys j in [i + N_kv - N_q - window + 1, i + N_kv - N_q].
+    Returns (O [B,H,N_q,d] bf16, LSE [B,H,N_q] fp32).  With i' = i + N_kv - N_q,
+    ``window > 0`` keeps keys j in [i' - window + 1, i'] when causal, and the
+    symmetric band [i' - window, i' + window] when not.
     Asynchronous on ``stream`` (default: torch's current stream).
     """
     lib = load_library()

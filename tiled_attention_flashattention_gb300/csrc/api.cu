@@ -133,8 +133,6 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, void *O, fl
     if (causal != 0 && causal != 1) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
     if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
     if (d != 64 && d != 128) return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: d must be 64 or 128");
-    if (window > 0 && !causal)
-        return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: a sliding window requires causal = 1");
     if (static_cast<long long>(B) * H * N_q > (1LL << 40) || static_cast<long long>(N_q) * d > (1LL << 31) ||
         static_cast<long long>(N_kv) * d > (1LL << 31))
         return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: problem too large");

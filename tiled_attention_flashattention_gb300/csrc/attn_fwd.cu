@@ -1,5 +1,5 @@
-// attn_fwd.cu -- fused attention forward (prefill), MHA/GQA, causal and causal
-// sliding window, for sm_103a.
+// attn_fwd.cu -- fused attention forward (prefill), MHA/GQA, causal, causal
+// sliding window and symmetric local window, for sm_103a.
 //
 // What is computed (TileLang 学习笔记, "FlashAttention 的实现" and its online
 // softmax formulas): for each query row, S = Q K^T over 128-key tiles, a
@@ -84,7 +84,9 @@ struct Params {
     __nv_bfloat16 *O;
     float *LSE;
     int B, H, H_kv, N_q, N_kv;
-    int causal, window;
+    // Visible keys of query row i, with i' = i + N_kv - N_q:
+    // i' - lo_pad <= j <= i' + hi_pad (and j < N_kv); kNoPad means unbounded.
+    int lo_pad, hi_pad;
     int group;          // H / H_kv
     int n_qblk;         // ceil(N_q / 256)
     float c;            // scale * log2(e)
@@ -100,11 +102,11 @@ struct Range {
 // KV tiles touched by query rows [r0, r1) (r1 > r0).
 __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
 {
-    const int off = p.N_kv - p.N_q;
-    const int key_hi = p.causal ? min(p.N_kv, r1 + off) : p.N_kv;          // exclusive
-    const int key_lo = p.window > 0 ? max(0, r0 + off - p.window + 1) : 0;  // inclusive
+    const long long off = static_cast<long long>(p.N_kv) - p.N_q;
+    const long long key_lo = max(0LL, r0 + off - p.lo_pad);                                   // inclusive
+    const long long key_hi = min(static_cast<long long>(p.N_kv), r1 - 1 + off + p.hi_pad + 1);  // exclusive
     if (key_hi <= key_lo) return {0, 0};
-    return {key_lo / kBN, (key_hi + kBN - 1) / kBN};
+    return {static_cast<int>(key_lo / kBN), static_cast<int>((key_hi + kBN - 1) / kBN)};
 }
 
 template <int D>
@@ -324,9 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tbase + lane_base + C::col_o(t);
         const float cexp = p.c;
         const float thr = kRescaleLog2 / cexp;     // threshold in raw score units
-        const int off = p.N_kv - p.N_q;
-        const int key_max = row + off;             // causal: keys <= key_max
-        const int key_min = row + off - p.window + 1;
+        const long long off = static_cast<long long>(p.N_kv) - p.N_q;
+        // this row's visible keys: key_min <= key <= key_max (key_max < N_kv)
+        const int key_max = static_cast<int>(min(row + off + p.hi_pad, static_cast<long long>(p.N_kv) - 1));
+        const int key_min = static_cast<int>(max(row + off - p.lo_pad, -1LL));
 
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
@@ -343,15 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
 
             const int k0 = j * kBN;
-            const bool need_mask = (k0 + kBN > p.N_kv) ||
-                                   (p.causal && k0 + kBN - 1 > r0[t] + off) ||
-                                   (p.window > 0 && k0 < (r1[t] - 1) + off - p.window + 1);
+            const bool need_mask = (k0 + kBN > p.N_kv) || (k0 + kBN - 1 > r0[t] + off + p.hi_pad) ||
+                                   (k0 < (r1[t] - 1) + off - p.lo_pad);
             if (need_mask) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i) {
                     const int key = k0 + i;
-                    const bool allowed = key < p.N_kv && (!p.causal || key <= key_max) &&
-                                         (p.window <= 0 || key >= key_min);
+                    const bool allowed = key >= key_min && key <= key_max;
                     if (!allowed) s[i] = -INFINITY;
                 }
             }
@@ -520,8 +521,14 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
     p.H_kv = H_kv;
     p.N_q = N_q;
     p.N_kv = N_kv;
-    p.causal = causal;
-    p.window = window > 0 ? window : 0;
+    constexpr int kNoPad = 1 << 30;
+    if (causal) {
+        p.hi_pad = 0;
+        p.lo_pad = window > 0 ? window - 1 : kNoPad;
+    } else {
+        p.hi_pad = window > 0 ? window : kNoPad;   // symmetric local window
+        p.lo_pad = window > 0 ? window : kNoPad;
+    }
     p.group = H / H_kv;
     p.n_qblk = (N_q + kQTiles * kBM - 1) / (kQTiles * kBM);
     p.c = scale * 1.4426950408889634f;

@@ -57,8 +57,8 @@ class MlaCase:
         return 1.0 / math.sqrt(self.d_c + self.d_r) if math.isnan(self.scale) else self.scale
 
 
-# The five named workloads (index = seed offset), plus the window variant of
-# the GQA one, which shares its inputs.
+# The five named workloads (index = seed offset), plus the causal-window and
+# symmetric-window variants of the GQA one, which share its inputs.
 WORKLOADS = {
     "mha_b1_h2_n128_d64": PrefillCase("mha_b1_h2_n128_d64", 1, 2, 2, 128, 128, 64, False,
                                       seed=SEED_BASE + 0),
@@ -69,6 +69,9 @@ WORKLOADS = {
     "gqa_window256_b2_h32_hkv8_n8192_d128": PrefillCase("gqa_window256_b2_h32_hkv8_n8192_d128", 2, 32,
                                                         8, 8192, 8192, 128, True, window=256,
                                                         seed=SEED_BASE + 2),
+    "gqa_swindow256_b2_h32_hkv8_n8192_d128": PrefillCase("gqa_swindow256_b2_h32_hkv8_n8192_d128", 2, 32,
+                                                         8, 8192, 8192, 128, False, window=256,
+                                                         seed=SEED_BASE + 2),
     "mla_decode_b64_h128_nkv4096": MlaCase("mla_decode_b64_h128_nkv4096", 64, 128, 4096,
                                            seed=SEED_BASE + 3),
     "mha_causal_spiky_b1_h32_n16384_d128": PrefillCase("mha_causal_spiky_b1_h32_n16384_d128", 1, 32,
