@@ -49,6 +49,8 @@ def _load():
             lib.oracle_attn_fwd.restype = I
             lib.oracle_mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, P, I64, I]
             lib.oracle_mla_decode.restype = I
+            lib.oracle_mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D, P, I64, I]
+            lib.oracle_mla_decode_paged.restype = I
             _lib = lib
     return _lib
 
@@ -129,6 +131,40 @@ def mla_decode(Q_nope, Q_pe, KV_latent, K_pe, scale: float, rows=None, threads: 
         threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_mla_decode rejected its arguments")
+    if rows is None:
+        O = O.reshape(B, H, d_c)
+        LSE = LSE.reshape(B, H)
+    return O, LSE
+
+
+def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, scale: float, rows=None,
+                     threads: int | None = None):
+    """Reference MLA decode over a paged KV cache: Q_nope [B,H,d_c], Q_pe [B,H,d_r]
+    (bf16), KV_cache [num_pages,page,d_c], K_pe_cache [num_pages,page,d_r] (bf16),
+    block_table [B,max_pages] and seqlens [B] (int32).  Key j of sequence b is row
+    j % page of page block_table[b, j // page].  Returns (O [B,H,d_c], LSE [B,H])
+    float64, or the listed flat rows b*H + h only."""
+    B, H, d_c = Q_nope.shape
+    d_r = Q_pe.shape[-1]
+    num_pages, page, _ = KV_cache.shape
+    max_pages = block_table.shape[1]
+    qn, qp, kv, kp = (_bf16_bits(x) for x in (Q_nope, Q_pe, KV_cache, K_pe_cache))
+    table = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    if rows is None:
+        n = B * H
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = rows_arr.shape[0]
+    O = np.zeros((n, d_c), dtype=np.float64)
+    LSE = np.zeros((n,), dtype=np.float64)
+    rc = _load().oracle_mla_decode_paged(
+        _ptr(qn), _ptr(qp), _ptr(kv), _ptr(kp), _ptr(table), _ptr(lens), _ptr(O), _ptr(LSE), B, H,
+        num_pages, max_pages, page, d_c, d_r, float(scale),
+        _ptr(rows_arr) if rows_arr is not None else None, n, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_mla_decode_paged rejected its arguments")
     if rows is None:
         O = O.reshape(B, H, d_c)
         LSE = LSE.reshape(B, H)

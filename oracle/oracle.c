@@ -266,3 +266,97 @@ int oracle_mla_decode(const uint16_t *Q_nope, const uint16_t *Q_pe, const uint16
     free(jobs);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* MLA decode over a paged KV cache with per-sequence lengths (the loop bound */
+/* of the FlashMLA article's section 2.2, ceildiv(seqlen_kv, block_N), taken  */
+/* per sequence).  Key j < seqlens[b] of sequence b is row j % page of page   */
+/* block_table[b * max_pages + j / page] of the caches                        */
+/*   KV_cache [num_pages][page][d_c],  K_pe_cache [num_pages][page][d_r];     */
+/* otherwise the same definition as oracle_mla_decode.  A sequence of length  */
+/* 0 has O = 0 and LSE = -inf.                                                */
+
+typedef struct {
+    const uint16_t *Qn, *Qp, *KV, *Kp;
+    const int32_t *table, *seqlens;
+    double *O, *LSE;
+    int B, H, max_pages, page, d_c, d_r;
+    double scale;
+    const int64_t *rows;   /* flat b*H + h, or NULL */
+    int64_t n_rows;
+    int n_threads, tid;
+} mla_paged_job;
+
+static void *mla_paged_worker(void *arg)
+{
+    const mla_paged_job *J = (const mla_paged_job *)arg;
+    const int dc = J->d_c, dr = J->d_r;
+    const long cap = (long)J->max_pages * J->page;
+    double *s = (double *)malloc(sizeof(double) * (cap > 0 ? cap : 1));
+    uint16_t *kv = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(cap > 0 ? cap : 1) * dc);
+    uint16_t *kp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(cap > 0 ? cap : 1) * dr);
+    if (!s || !kv || !kp) {
+        free(s);
+        free(kv);
+        free(kp);
+        return (void *)1;
+    }
+    for (int64_t k = J->tid; k < J->n_rows; k += J->n_threads) {
+        int64_t flat = J->rows ? J->rows[k] : k;
+        long b = (long)(flat / J->H), h = (long)(flat % J->H);
+        const long n = J->seqlens[b];
+        /* gather this sequence's key rows in order */
+        for (long j = 0; j < n; j++) {
+            const long pg = J->table[b * J->max_pages + j / J->page];
+            const long r = pg * J->page + j % J->page;
+            memcpy(kv + j * dc, J->KV + r * dc, sizeof(uint16_t) * dc);
+            memcpy(kp + j * dr, J->Kp + r * dr, sizeof(uint16_t) * dr);
+        }
+        const uint16_t *qn = J->Qn + (b * J->H + h) * dc;
+        const uint16_t *qp = J->Qp + (b * J->H + h) * dr;
+        for (long j = 0; j < n; j++) {
+            double nope = 0.0, rope = 0.0;
+            for (int c = 0; c < dc; c++) nope += bf16_to_f64(qn[c]) * bf16_to_f64(kv[j * dc + c]);
+            for (int c = 0; c < dr; c++) rope += bf16_to_f64(qp[c]) * bf16_to_f64(kp[j * dr + c]);
+            s[j] = J->scale * (nope + rope);
+        }
+        softmax_weighted_sum(s, n, kv, dc, dc, J->O + k * dc, J->LSE + k, NULL);
+    }
+    free(s);
+    free(kv);
+    free(kp);
+    return NULL;
+}
+
+int oracle_mla_decode_paged(const uint16_t *Q_nope, const uint16_t *Q_pe, const uint16_t *KV_cache,
+                            const uint16_t *K_pe_cache, const int32_t *block_table, const int32_t *seqlens,
+                            double *O, double *LSE, int B, int H, int num_pages, int max_pages, int page,
+                            int d_c, int d_r, double scale, const int64_t *rows, int64_t n_rows, int n_threads)
+{
+    if (B < 0 || H <= 0 || num_pages < 0 || max_pages < 0 || page <= 0 || d_c <= 0 || d_r < 0) return -1;
+    for (int b = 0; b < B; b++) {
+        if (seqlens[b] < 0 || (long)seqlens[b] > (long)max_pages * page) return -1;
+        for (long j = 0; j < seqlens[b]; j += page) {
+            const int32_t pg = block_table[(long)b * max_pages + j / page];
+            if (pg < 0 || pg >= num_pages) return -1;
+        }
+    }
+    int64_t total = (int64_t)B * H;
+    if (!rows) n_rows = total;
+    if (n_rows == 0) return 0;
+    for (int64_t k = 0; rows && k < n_rows; k++)
+        if (rows[k] < 0 || rows[k] >= total) return -1;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > n_rows) n_threads = (int)n_rows;
+
+    mla_paged_job *jobs = (mla_paged_job *)malloc(sizeof(mla_paged_job) * n_threads);
+    if (!jobs) return -1;
+    for (int t = 0; t < n_threads; t++) {
+        mla_paged_job j = {Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, O, LSE, B, H,
+                           max_pages, page, d_c, d_r, scale, rows, n_rows, n_threads, t};
+        jobs[t] = j;
+    }
+    int rc = run_threads(mla_paged_worker, jobs, sizeof(mla_paged_job), n_threads);
+    free(jobs);
+    return rc;
+}

@@ -296,6 +296,66 @@ def test_mla_rows_subset():
     np.testing.assert_array_equal(Ls, LSE.reshape(-1)[[1, 4]])
 
 
+def _dense_as_paged(KV, Kp, page):
+    """The dense [B,N,d] caches as pages in order: sequence b owns pages b*N/page ..."""
+    B, N, d_c = KV.shape
+    n = N // page
+    table = torch.arange(B * n, dtype=torch.int32).reshape(B, n)
+    return KV.reshape(B * n, page, d_c), Kp.reshape(B * n, page, Kp.shape[-1]), table
+
+
+def test_mla_paged_contiguous_pages_equal_dense():
+    Qn, Qp, KV, Kp = wl.random_mla(3, 8, 256, 512, 64, seed=30)
+    O, L = oracle.mla_decode(Qn, Qp, KV, Kp, 0.04)
+    KVc, Kpc, table = _dense_as_paged(KV, Kp, 64)
+    Op, Lp = oracle.mla_decode_paged(Qn, Qp, KVc, Kpc, table, [256] * 3, 0.04)
+    np.testing.assert_array_equal(O, Op)
+    np.testing.assert_array_equal(L, Lp)
+
+
+def test_mla_paged_invariant_to_page_placement():
+    Qn, Qp, KV, Kp, table, lens = wl.random_mla_paged(4, [130, 64, 1, 200], d_c=64, d_r=16, page=64, seed=31)
+    O1, L1 = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, lens, 0.1)
+    perm = torch.randperm(KV.shape[0], generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    table2 = torch.where(table >= 0, inv[table.clamp(min=0).long()].to(torch.int32), table)
+    O2, L2 = oracle.mla_decode_paged(Qn, Qp, KV[perm].contiguous(), Kp[perm].contiguous(), table2, lens, 0.1)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+
+
+def test_mla_paged_lengths_truncate_the_sequence():
+    lens = [1, 63, 64, 65, 190]
+    Qn, Qp, KV, Kp, table, L = wl.random_mla_paged(4, lens, d_c=64, d_r=16, page=64, seed=32)
+    O, LSE = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, 0.1)
+    for b, n in enumerate(lens):
+        rows = torch.arange(n)
+        pages = table[b, rows // 64].long()
+        kv = KV[pages, rows % 64].unsqueeze(0).contiguous()
+        kp = Kp[pages, rows % 64].unsqueeze(0).contiguous()
+        Od, Ld = oracle.mla_decode(Qn[b:b + 1].contiguous(), Qp[b:b + 1].contiguous(), kv, kp, 0.1)
+        np.testing.assert_array_equal(O[b], Od[0])
+        np.testing.assert_array_equal(LSE[b], Ld[0])
+
+
+def test_mla_paged_empty_sequence():
+    Qn, Qp, KV, Kp, table, lens = wl.random_mla_paged(2, [0, 70], d_c=64, d_r=16, page=64, seed=33)
+    O, L = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, lens, 0.1)
+    assert (O[0] == 0).all() and np.isneginf(L[0]).all()
+    assert np.isfinite(L[1]).all()
+
+
+def test_mla_paged_rejects_bad_tables():
+    Qn, Qp, KV, Kp, table, lens = wl.random_mla_paged(2, [70, 10], d_c=64, d_r=16, page=64, seed=34)
+    with pytest.raises(ValueError):
+        oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, [129, 10], 0.1)      # longer than the table
+    bad = table.clone()
+    bad[0, 1] = KV.shape[0]
+    with pytest.raises(ValueError):
+        oracle.mla_decode_paged(Qn, Qp, KV, Kp, bad, lens, 0.1)             # page out of the pool
+
+
 def test_rejects_bad_arguments():
     Q, K, V = wl.random_prefill(1, 3, 2, 4, 4, 8, seed=18)  # H % H_kv != 0
     with pytest.raises(ValueError):

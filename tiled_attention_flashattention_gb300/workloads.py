@@ -127,3 +127,29 @@ def random_mla(B, H, N_kv, d_c, d_r, seed):
     shapes = [(B, H, d_c), (B, H, d_r), (B, N_kv, d_c), (B, N_kv, d_r)]
     return tuple(torch.randn(*s, generator=g, dtype=torch.float32).to(torch.bfloat16)
                  for s in shapes)
+
+
+def random_mla_paged(H, seqlens, d_c=512, d_r=64, page=64, spare_pages=3, seed=0):
+    """Paged MLA decode inputs: Q_nope [B,H,d_c], Q_pe [B,H,d_r] (bf16),
+    KV_cache [num_pages,page,d_c], K_pe_cache [num_pages,page,d_r] (bf16),
+    block_table [B,max_pages] int32, seqlens [B] int32.  Each sequence gets
+    ceil(len / page) pages drawn without replacement from a pool with
+    `spare_pages` unused pages (random placement); unused table entries are -1.
+    Same drawing recipe (torch CPU generator, N(0,1) -> bf16)."""
+    g = _gen(seed)
+    lens = [int(x) for x in seqlens]
+    B = len(lens)
+    need = [(n + page - 1) // page for n in lens]
+    max_pages = max(1, max(need) if need else 1)
+    num_pages = sum(need) + spare_pages
+    Qn = torch.randn(B, H, d_c, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    Qp = torch.randn(B, H, d_r, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    KV = torch.randn(num_pages, page, d_c, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    Kp = torch.randn(num_pages, page, d_r, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, generator=g)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n].to(torch.int32)
+        k += n
+    return Qn, Qp, KV, Kp, table, torch.tensor(lens, dtype=torch.int32)
