@@ -116,6 +116,47 @@ int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, cons
                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * mla_decode_paged_workspace_bytes -- size of the scratch buffer
+ * mla_decode_paged needs for B sequences on the current device (it depends
+ * on the device's SM count, not on the lengths).  Returns 0 for an invalid
+ * shape.
+ */
+size_t mla_decode_paged_workspace_bytes(int B, int H, int d_c);
+
+/*
+ * mla_decode_paged -- MLA decode over a paged KV cache, each sequence with
+ * its own length.
+ *
+ * Operation: mla_decode's, with the FlashMLA article's KV loop bound
+ * (section 2.2, ceildiv(seqlen_kv, block_N)) taken per sequence: sequence b
+ * has keys j < cache_seqlens[b], and key j is row j % 64 of page
+ * block_table[b * max_pages_per_seq + j / 64] of the caches.  A sequence of
+ * length 0 gets O = 0 and LSE = -inf.
+ *
+ * Arguments
+ *   Q_nope bf16 [B, H, d_c]   Q_pe bf16 [B, H, d_r]
+ *   KV_cache bf16 [num_pages, 64, d_c]   K_pe_cache bf16 [num_pages, 64, d_r]
+ *   block_table int32 [B, max_pages_per_seq] (device; entries past a
+ *     sequence's last page are not read)
+ *   cache_seqlens int32 [B] (device; 0 <= len <= 64 * max_pages_per_seq)
+ *   O bf16 [B, H, d_c] (written)    LSE fp32 [B, H] (written)
+ *   page_size = 64, d_c = 512, d_r = 64, H = 128, B >= 1, num_pages >= 1,
+ *   max_pages_per_seq >= 1, scale finite and > 0.
+ *   workspace: device buffer of at least mla_decode_paged_workspace_bytes(B,
+ *   H, d_c) bytes, 16-byte aligned, owned by the caller, overwritten; calls
+ *   that share a workspace must not overlap in time.
+ * Rows of a sequence's last page past its length may hold anything (they
+ * are zeroed on chip before the P V product).  The lengths are read on the
+ * device: one outside [0, 64 * max_pages_per_seq] is clamped and reported by
+ * the next gbattn_check as GBATTN_ERR_INVALID_ARG.  A block-table entry
+ * outside [0, num_pages) reads zeros.
+ */
+int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
+                     const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
+                     int num_pages, int max_pages_per_seq, int page_size, int d_c, int d_r, float scale,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart of this entry point; it is a
  * convenience of this library.

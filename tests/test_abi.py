@@ -72,3 +72,21 @@ def test_mla_decode_argument_errors(lib):
     assert mla(d_c=256) == 2
     assert mla(Qn=0) == 1
     assert mla(Qn=40) == 3
+
+
+def test_mla_decode_paged_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def paged(B=2, H=128, num_pages=4, max_pages=2, page=64, d_c=512, d_r=64, scale=0.04, Qn=16, table=16,
+              lens=16, ws=16):
+        return lib.mla_decode_paged(vp(Qn), vp(16), vp(16), vp(16), vp(table), vp(lens), vp(16), vp(16), B, H,
+                                    num_pages, max_pages, page, d_c, d_r, ctypes.c_float(scale), vp(ws), 1 << 20,
+                                    None)
+    assert paged(B=0) == 1
+    assert paged(num_pages=0) == 1
+    assert paged(scale=0.0) == 1
+    assert paged(page=32) == 2                     # page size other than 64
+    assert paged(H=64) == 2
+    assert paged(table=0) == 1                     # null block table
+    assert paged(lens=18) == 3                     # misaligned lengths
+    assert paged(Qn=40) == 3

@@ -105,7 +105,12 @@ struct Params {
     float *ws_LSE;      // [slots][128]
     int B, N_kv, ntile;
     long long T;        // B * ntile
-    int C;              // clusters
+    int C;              // clusters launched (the tiles are split over min(C, T) of them)
+    // Paged form only (sequences of their own lengths, 64-key pages):
+    const int *tile_start;    // [B + 1] first flat tile of each sequence; tile_start[B] = all tiles
+    const int *seq_len;       // [B] keys of each sequence (clamped to the block table's capacity)
+    const int *block_table;   // [B][max_pages] page of each 64-key tile
+    int max_pages;
     int max_seg;        // workspace slots per cluster (2: its first and last range)
     float c;            // scale * log2(e)
     int *status;
@@ -124,6 +129,53 @@ __host__ __device__ __forceinline__ int cluster_of_tile(long long x, long long T
     return static_cast<int>(((x + 1) * C - 1) / T);
 }
 
+// Where each sequence's key tiles sit in the flat tile space: dense (every
+// sequence N_kv keys, B * ntile tiles) or paged (per-sequence lengths, prefix
+// sums computed on the device by mla_tiles_kernel).
+template <bool kPaged>
+struct SeqMap {
+    const Params &p;
+    // first flat tile of sequence b (b <= B)
+    __device__ __forceinline__ long long start(int b) const
+    {
+        if constexpr (kPaged)
+            return p.tile_start[b];
+        else
+            return static_cast<long long>(b) * p.ntile;
+    }
+    __device__ __forceinline__ int keys(int b) const
+    {
+        if constexpr (kPaged)
+            return p.seq_len[b];
+        else
+            return p.N_kv;
+    }
+    // the sequence holding flat tile x (0 <= x < total()); empty sequences own no tile
+    __device__ __forceinline__ int of_tile(long long x) const
+    {
+        if constexpr (kPaged) {
+            int lo = 0, hi = p.B;      // the last b with start(b) <= x
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.tile_start[mid] <= x)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            return lo;
+        } else {
+            return static_cast<int>(x / p.ntile);
+        }
+    }
+    __device__ __forceinline__ long long total() const
+    {
+        if constexpr (kPaged)
+            return p.tile_start[p.B];
+        else
+            return p.T;
+    }
+};
+
 __device__ __forceinline__ void bulk_wait_read_allow1()
 {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -139,10 +191,12 @@ __device__ __forceinline__ void issue_s(uint32_t d, uint32_t a, uint64_t kvd, ui
         umma_ts(d, a + k * 8, desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idesc, k > 0 ? 1u : 0u);
 }
 
+template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
                      const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp, const Params p)
 {
+    const SeqMap<kPaged> S{p};
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -154,11 +208,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int cl = blockIdx.x / 2;
-    const long long t_begin = range_start(cl, p.T, p.C), t_end = range_start(cl + 1, p.T, p.C);
+    const long long T = S.total();
+    // Partition over min(C, T) clusters, so that no cluster inside a split
+    // sequence's span is empty; the clusters past that have no work.
+    const int Ce = static_cast<int>(min(static_cast<long long>(p.C), T));
+    const long long t_begin = cl < Ce ? range_start(cl, T, Ce) : T;
+    const long long t_end = cl < Ce ? range_start(cl + 1, T, Ce) : T;
     const int nch = rank == 0 ? 4 : 5;              // contraction chunks of this CTA
     const int dim0 = static_cast<int>(rank) * kHalf;
-    const int b_first = static_cast<int>(t_begin / p.ntile);
-    const int b_last = t_end > t_begin ? static_cast<int>((t_end - 1) / p.ntile) : b_first - 1;
+    // first and last sequence with tiles in this cluster's range (none when empty)
+    const int b_first = t_end > t_begin ? S.of_tile(t_begin) : 0;
+    const int b_last = t_end > t_begin ? S.of_tile(t_end - 1) : -1;
 
     if (threadIdx.x == 0) {
         mbar_init(&c.q_full, 128);
@@ -208,8 +268,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t kvbytes = nch * kKvChunk;
             const uint32_t qbytes = rank == 0 ? 2 * kQChunk : 2 * kQChunk + kQChunk / 2;
             for (int b = b_first; b <= b_last && ok; ++b) {
-                const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
-                const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+                const long long P0 = S.start(b);
+                const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
+                if (x0 >= x1) continue;       // an empty sequence
+                const int *pages = kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
                 // This sequence's query part: two ring slots, each [128 heads x 64 dims]
                 // chunks 2i and 2i + 1 of Q_nope, plus heads [64i, 64i + 64) of Q_pe on CTA 1.
                 for (int qi = 0; qi < 2; ++qi) {
@@ -233,22 +295,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tma_prefetch_l2_3d(&tmQp, 0, 0, b + 1);
                             tma_prefetch_l2_3d(&tmQp, 0, 64, b + 1);
                         }
-                        const int nn = static_cast<int>(min(static_cast<long long>(p.ntile), t_end - x1));
-                        for (int j = 0; j < min(nn, 3); ++j) {
-                            for (int ch = 0; ch < 4; ++ch)
-                                tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, j * kBN, b + 1);
-                            if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, j * kBN, b + 1);
+                        if constexpr (!kPaged) {
+                            const int nn = static_cast<int>(min(static_cast<long long>(p.ntile), t_end - x1));
+                            for (int j = 0; j < min(nn, 3); ++j) {
+                                for (int ch = 0; ch < 4; ++ch)
+                                    tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, j * kBN, b + 1);
+                                if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, j * kBN, b + 1);
+                            }
                         }
                     }
-                    const int key0 = static_cast<int>(x - static_cast<long long>(b) * p.ntile) * kBN;
+                    const int tile = static_cast<int>(x - P0);          // tile of the sequence
+                    // dense: rows [64 tile, 64 tile + 64) of sequence b; paged: the tile's page
+                    // (read before the slot wait, so the load overlaps it)
+                    const int row0 = kPaged ? 0 : tile * kBN;
+                    const int outer = kPaged ? __ldg(pages + tile) : b;
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], kvbytes);
                     for (int ch = 0; ch < 4; ++ch)
-                        tma_load_3d(dst + ch * kKvChunk, &tmKV, &c.full[s], dim0 + ch * 64, key0, b);
-                    if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, key0, b);
+                        tma_load_3d(dst + ch * kKvChunk, &tmKV, &c.full[s], dim0 + ch * 64, row0, outer);
+                    if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, row0, outer);
                     ++it;
                 }
             }
@@ -272,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // behind the softmax of an earlier unit.  Readiness is polled
             // without suspending the thread.
             const int total = static_cast<int>(t_end - t_begin);
-            const long long bnd0 = (t_begin / p.ntile + 1) * p.ntile;   // first segment boundary
+            const long long bnd0 = S.start(b_first + 1);   // end of the first sequence's tiles
             // Ring slots: each range of the cluster starts with two query slots,
             // then one slot per key tile.
             // S cursor: tile gs (flat t_begin + gs), its ring slot and segment.
@@ -310,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             ++u_slot;
                             if (++u_x == u_bnd) {
                                 u_slot += 2;
-                                u_bnd += p.ntile;
+                                if (u_x < t_end) u_bnd = S.start(S.of_tile(u_x) + 1);
                                 ++u_seg;
                                 u_first = true;
                             } else {
@@ -341,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ++s_slot;
                         if (s_x == s_bnd) {
                             s_slot += 2;
-                            s_bnd += p.ntile;
+                            if (s_x < t_end) s_bnd = S.start(S.of_tile(s_x) + 1);
                             ++s_seg;
                             s_first = true;
                         } else {
@@ -421,13 +489,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_arrive(&c.q_full);
             return true;
         };
-        bool ok = load_q(0);
+        bool ok = b_last < b_first || load_q(0);
         uint32_t t = 0;          // tiles of this CTA so far
-        int seg = 0;
-        for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
-            const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
-            const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+        int seg = 0;             // non-empty sequences of this CTA so far
+        for (int b = b_first; b <= b_last && ok; ++b) {
+            const long long P0 = S.start(b);
+            const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
             const int n = static_cast<int>(x1 - x0);
+            if (n <= 0) continue;         // an empty sequence
             for (int i = 0; i < n && ok; ++i, ++t) {
                 if (!(ok = barrier_and(kBarX, 128, mbar_wait(&c.s_full, t & 1u, ctl)))) break;
                 tc_fence_after_sync();
@@ -435,6 +504,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_ld_x64(tbase + lane_base + kColS, sr);
                 tc_fence_before_sync();
                 mbar_arrive(&c.s_free);
+                if constexpr (kPaged) {
+                    // The sequence ends inside this tile: the rows past its end hold
+                    // whatever the page holds, and P = 0 there does not cancel a
+                    // non-finite V.  Zero them (latent chunks) before the P V MMAs,
+                    // which run after this CTA's softmax, which waits for the sends.
+                    const int valid = S.keys(b) - static_cast<int>(x0 - P0 + i) * kBN;
+                    if (valid < kBN) {
+                        uint8_t *stage = sKV + ((2 * (seg + 1) + static_cast<int>(t)) % kStages) * kStageBytes;
+                        const int pieces = (kBN - valid) * 8;        // 16-byte pieces per chunk
+                        for (int k = threadIdx.x - 128; k < 4 * pieces; k += 128) {
+                            const int ch = k / pieces, r = valid + (k % pieces) / 8, q = k % 8;
+                            *reinterpret_cast<uint4 *>(stage + ch * kKvChunk + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
                 if (i == n - 1 && b < b_last) {
                     // The range's last S is done, and with it every read of its query:
                     // load the next range's query now, so that its first S does not
@@ -473,6 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            ++seg;
         }
         if (leader) bulk_wait_all();   // no copy of this CTA may still be writing to the peer
     } else if (warp >= 8) {
@@ -491,10 +576,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool okw = true;         // this warp's waits so far (agreed on at the next barrier)
         uint32_t t = 0;
         int seg = 0;
-        for (int b = b_first; b <= b_last && ok; ++b, ++seg) {
-            const long long x0 = max(t_begin, static_cast<long long>(b) * p.ntile);
-            const long long x1 = min(t_end, static_cast<long long>(b + 1) * p.ntile);
+        for (int b = b_first; b <= b_last && ok; ++b) {
+            const long long P0 = S.start(b), P1 = S.start(b + 1);
+            const long long x0 = max(t_begin, P0), x1 = min(t_end, P1);
             const int n = static_cast<int>(x1 - x0);
+            if (n <= 0) continue;         // an empty sequence
+            const int n_keys = S.keys(b);
+            ++seg;
             float m_ref = -INFINITY, l = 0.f;
             for (int i = 0; i < n && ok; ++i, ++t) {
 #pragma unroll 1
@@ -521,11 +609,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mbar_arrive_remote(peer_xfree[h]);
                     }
 
-                    const int key0 = static_cast<int>(x0 + i - static_cast<long long>(b) * p.ntile) * kBN + h * kBU;
-                    if (key0 + kBU > p.N_kv) {
+                    const int key0 = static_cast<int>(x0 + i - P0) * kBN + h * kBU;
+                    if (key0 + kBU > n_keys) {
 #pragma unroll
                         for (int k = 0; k < kBU; ++k)
-                            if (key0 + k >= p.N_kv) s[k] = -INFINITY;
+                            if (key0 + k >= n_keys) s[k] = -INFINITY;
                     }
                     float mx = s[0];
 #pragma unroll
@@ -574,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // ---- epilogue of this range of sequence b (after its last PV)
             if (!(ok = barrier_and(kBarS, 128, mbar_wait(&c.pfree[1], (t - 1) & 1u, ctl) && okw))) break;
             tc_fence_after_sync();
-            const bool whole = (n == p.ntile);
+            const bool whole = (x1 - x0 == P1 - P0);
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             const float lse = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
             const size_t slot = static_cast<size_t>(cl) * 2 + (b == b_first ? 0 : 1);
@@ -622,20 +710,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Merge the parts of each split sequence: LSE = ln sum_q e^{LSE_q},
 // O = sum_q e^{LSE_q - LSE} (O_q / l_q).  One block per (sequence, group of 16
 // heads), 256 threads, 32 output dims per thread; sequences written whole by
-// the split kernel are skipped.  Up to three parts (the usual case) every
-// load of a thread is issued at once.
+// the split kernel are skipped, and (paged form) a sequence of length 0 gets
+// O = 0, LSE = -inf.  Up to three parts (the usual case) every load of a
+// thread is issued at once.
+template <bool kPaged>
 __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the split kernel is complete
+    const SeqMap<kPaged> S{p};
     const int b = blockIdx.x / 8, hg = blockIdx.x % 8;
-    const long long x0 = static_cast<long long>(b) * p.ntile;
-    const int c0 = cluster_of_tile(x0, p.T, p.C);
-    const int c1 = cluster_of_tile(x0 + p.ntile - 1, p.T, p.C);
-    if (c0 == c1) return;
     const int h = hg * 16 + threadIdx.x / 16;
     const int d0 = (threadIdx.x % 16) * 32;
+    const long long T = S.total();
+    const long long x0 = S.start(b), x1 = S.start(b + 1);
+    if (x1 <= x0) {
+        uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * kH + h) * kDc + d0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+        if (threadIdx.x % 16 == 0) p.LSE[static_cast<size_t>(b) * kH + h] = -INFINITY;
+        return;
+    }
+    const int Ce = static_cast<int>(min(static_cast<long long>(p.C), T));   // clusters with work
+    const int c0 = cluster_of_tile(x0, T, Ce);
+    const int c1 = cluster_of_tile(x1 - 1, T, Ce);
+    if (c0 == c1) return;
     auto slot_of = [&](int q) -> size_t {
-        return static_cast<size_t>(q) * 2 + (b == range_start(q, p.T, p.C) / p.ntile ? 0 : 1);
+        return static_cast<size_t>(q) * 2 + (b == S.of_tile(range_start(q, T, Ce)) ? 0 : 1);
     };
     auto accumulate = [](float (&acc)[32], float w, const uint4 (&v)[4]) {
 #pragma unroll
@@ -701,6 +801,56 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     if (threadIdx.x % 16 == 0) p.LSE[static_cast<size_t>(b) * kH + h] = lse;
 }
 
+// Paged form: per-sequence key counts (clamped to the block table's capacity;
+// a length outside [0, capacity] sets the status word) and the exclusive
+// prefix sum of their 64-key tile counts, tile_start[0..B].  One block.
+__global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlens, int *seq_len, int *tile_start,
+                                                        int B, int capacity, int *status)
+{
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += 1024) {
+        const int b = base + threadIdx.x;
+        int n = 0;
+        if (b < B) {
+            int len = cache_seqlens[b];
+            if (len < 0 || len > capacity) {
+                atomicCAS(status, 0, kStatusBadLength);
+                len = min(max(len, 0), capacity);
+            }
+            seq_len[b] = len;
+            n = (len + kBN - 1) / kBN;
+        }
+        int v = n;                          // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane == 31) warp_sum[warp] = v;
+        __syncthreads();
+        if (warp == 0) {                    // inclusive scan of the warp totals
+            int w = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sum[lane] = w;
+        }
+        __syncthreads();
+        const int incl = carry + (warp > 0 ? warp_sum[warp - 1] : 0) + v;
+        if (b < B) tile_start[b] = incl - n;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) tile_start[B] = carry;
+}
+
 struct Plan {
     int ntile, C, max_seg;
     long long T;
@@ -714,7 +864,7 @@ int resident_clusters(int num_sms)
     static int cached = -1;
     if (cached > 0) return cached;
     int n = 0;
-    if (cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -727,7 +877,7 @@ int resident_clusters(int num_sms)
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, mla_split_kernel, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla_split_kernel<false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (n <= 0) n = num_sms / 2;
@@ -849,10 +999,14 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     p.c = scale * 1.4426950408889634f;
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    p.tile_start = nullptr;
+    p.seq_len = nullptr;
+    p.block_table = nullptr;
+    p.max_pages = 0;
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
-        mla_split_kernel<<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, tqn, tqp, p);
+        mla_split_kernel<false><<<2 * pl.C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, tqn, tqp, p);
         e = cudaGetLastError();
     }
     bool split = false;   // does a cluster range boundary fall inside a sequence?
@@ -867,10 +1021,92 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
         attr.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+        e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<false>, p);
     }
     if (e != cudaSuccess) {
         err = std::string("mla_decode launch: ") + cudaGetErrorString(e);
+        return 5;
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------- paged form
+// Workspace: split partials as in the dense form (2 slots per cluster), then
+// tile_start [B + 1] and seq_len [B] (int32).
+static size_t paged_bytes(int B, int clusters, size_t &off_tiles)
+{
+    const size_t slots = static_cast<size_t>(clusters) * 2;
+    off_tiles = slots * kH * kDc * sizeof(__nv_bfloat16) + slots * kH * sizeof(float);
+    return off_tiles + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
+}
+
+size_t mla_paged_workspace_bytes(int B, int H, int d_c, int num_sms)
+{
+    if (B < 1 || H != kH || d_c != kDc) return 0;
+    size_t off = 0;
+    return paged_bytes(B, resident_clusters(num_sms), off);
+}
+
+int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
+                            const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
+                            int num_pages, int max_pages, int d_c, int d_r, float scale, void *workspace,
+                            size_t workspace_bytes, const LaunchEnv &env, std::string &err)
+{
+    const int C = resident_clusters(env.num_sms);
+    size_t off_tiles = 0;
+    if (workspace_bytes < paged_bytes(B, C, off_tiles)) {
+        err = "mla_decode_paged: workspace too small";
+        return 4;
+    }
+    CUtensorMap tkv, tkp, tqn, tqp;
+    if (!make_tma_bf16_3d(tkv, KV_cache, d_c, kBN, num_pages, kBN, err) ||
+        !make_tma_bf16_3d(tkp, K_pe_cache, d_r, kBN, num_pages, kBN, err) ||
+        !make_tma_bf16_3d(tqn, Q_nope, d_c, kH, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
+        return 5;
+    const size_t slots = static_cast<size_t>(C) * 2;
+    Params p;
+    p.O = static_cast<__nv_bfloat16 *>(O);
+    p.LSE = LSE;
+    p.ws_O = static_cast<__nv_bfloat16 *>(workspace);
+    p.ws_LSE = reinterpret_cast<float *>(p.ws_O + slots * kH * kDc);
+    int *tile_start = reinterpret_cast<int *>(static_cast<char *>(workspace) + off_tiles);
+    int *seq_len = tile_start + B + 1;
+    p.B = B;
+    p.N_kv = 0;
+    p.ntile = 0;
+    p.T = 0;
+    p.C = C;
+    p.max_seg = 2;
+    p.c = scale * 1.4426950408889634f;
+    p.status = env.status;
+    p.timeout_ns = env.timeout_ns;
+    p.tile_start = tile_start;
+    p.seq_len = seq_len;
+    p.block_table = block_table;
+    p.max_pages = max_pages;
+    mla_tiles_kernel<<<1, 1024, 0, env.stream>>>(cache_seqlens, seq_len, tile_start, B, max_pages * kBN, env.status);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mla_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess) {
+        mla_split_kernel<true><<<2 * C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, tqn, tqp, p);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(B) * 8, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = env.stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<true>, p);
+    }
+    if (e != cudaSuccess) {
+        err = std::string("mla_decode_paged launch: ") + cudaGetErrorString(e);
         return 5;
     }
     return 0;

@@ -16,12 +16,6 @@
 
 namespace gbattn {
 
-// Device status word codes (first error wins).
-enum : int {
-    kStatusOk = 0,
-    kStatusWaitTimeout = 1,
-};
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
