@@ -270,6 +270,41 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def paged_decode_workload(gb, dev, peaks, flush, reps=10):
+    """Kernel-only HBM GB/s of mla_decode_paged on 64 sequences with seeded
+    lengths in [2048, 6144] keys (mean about 4096) in 64-key pages placed at
+    random (inputs resident, L2 flushed before each timed call).  Algorithmic
+    bytes: every key row read once (576 bf16), Q read once, O and LSE written
+    once."""
+    g = torch.Generator().manual_seed(wl.SEED_BASE + 5)
+    lens = torch.randint(2048, 6145, (64,), generator=g).tolist()
+    Qn, Qp, KV, Kp, table, L = (x.to(dev) for x in wl.random_mla_paged(128, lens, seed=wl.SEED_BASE + 5))
+    B, H = len(lens), 128
+    O = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty(B, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(gb.mla_decode_paged_workspace_bytes(B), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(576)
+    call = lambda: gb.mla_decode_paged(Qn, Qp, KV, Kp, table, L, scale=scale, O=O, LSE=LSE, workspace=ws)
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream(dev)
+    total = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    gb.check()
+    t = total / reps
+    by = float(sum(lens) * 576 * 2 + B * H * 576 * 2 + B * H * 512 * 2 + B * H * 4)
+    gbs = by / t / 1e9
+    return {"workload": "mla_paged_b64_h128_len2048to6144_page64", "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "ms": t * 1e3, "total_keys": int(sum(lens)), "algorithmic_bytes": by}
+
+
 def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
     """Kernel-only TFLOP/s of the other prefill workloads (inputs resident,
     L2 flushed before each timed launch, CUDA events around the launch)."""
@@ -449,6 +484,7 @@ def run_ours(args, rank, world, local):
     }
     if not args.no_extra:
         line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
+        line["decode_paged"] = paged_decode_workload(gb, dev, peaks, flush)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)

@@ -208,17 +208,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int cl = blockIdx.x / 2;
-    const long long T = S.total();
-    // Partition over min(C, T) clusters, so that no cluster inside a split
-    // sequence's span is empty; the clusters past that have no work.
-    const int Ce = static_cast<int>(min(static_cast<long long>(p.C), T));
-    const long long t_begin = cl < Ce ? range_start(cl, T, Ce) : T;
-    const long long t_end = cl < Ce ? range_start(cl + 1, T, Ce) : T;
     const int nch = rank == 0 ? 4 : 5;              // contraction chunks of this CTA
     const int dim0 = static_cast<int>(rank) * kHalf;
-    // first and last sequence with tiles in this cluster's range (none when empty)
-    const int b_first = t_end > t_begin ? S.of_tile(t_begin) : 0;
-    const int b_last = t_end > t_begin ? S.of_tile(t_end - 1) : -1;
 
     if (threadIdx.x == 0) {
         mbar_init(&c.q_full, 128);
@@ -255,6 +246,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The combine kernel may be scheduled as soon as SMs free up; it waits for
     // this grid's completion before reading anything.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Paged form: this grid is a programmatic dependent of the tile-table
+    // kernel; everything above overlapped it, the table is read below.
+    if constexpr (kPaged) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long T = S.total();
+    // Partition over min(C, T) clusters, so that no cluster inside a split
+    // sequence's span is empty; the clusters past that have no work.
+    const int Ce = static_cast<int>(min(static_cast<long long>(p.C), T));
+    const long long t_begin = cl < Ce ? range_start(cl, T, Ce) : T;
+    const long long t_end = cl < Ce ? range_start(cl + 1, T, Ce) : T;
+    // first and last sequence with tiles in this cluster's range (none when empty)
+    const int b_first = t_end > t_begin ? S.of_tile(t_begin) : 0;
+    const int b_last = t_end > t_begin ? S.of_tile(t_end - 1) : -1;
 
     if (warp == 0) {
         // =================== TMA producer ===================
@@ -272,6 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
                 if (x0 >= x1) continue;       // an empty sequence
                 const int *pages = kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+                // paged: the page of the next tile, loaded one tile ahead of its use
+                int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : b;
                 // This sequence's query part: two ring slots, each [128 heads x 64 dims]
                 // chunks 2i and 2i + 1 of Q_nope, plus heads [64i, 64i + 64) of Q_pe on CTA 1.
                 for (int qi = 0; qi < 2; ++qi) {
@@ -290,25 +295,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // The next range's query and first key tiles into L2 a few tiles
                         // ahead: its two query slots take half the ring, so its first
                         // tile is loaded late and must not also pay the HBM latency.
-                        for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmQn, dim0 + ch * 64, 0, b + 1);
+                        const int nb = S.of_tile(x1);          // the next sequence with tiles here
+                        for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmQn, dim0 + ch * 64, 0, nb);
                         if (rank == 1) {
-                            tma_prefetch_l2_3d(&tmQp, 0, 0, b + 1);
-                            tma_prefetch_l2_3d(&tmQp, 0, 64, b + 1);
+                            tma_prefetch_l2_3d(&tmQp, 0, 0, nb);
+                            tma_prefetch_l2_3d(&tmQp, 0, 64, nb);
                         }
-                        if constexpr (!kPaged) {
-                            const int nn = static_cast<int>(min(static_cast<long long>(p.ntile), t_end - x1));
-                            for (int j = 0; j < min(nn, 3); ++j) {
-                                for (int ch = 0; ch < 4; ++ch)
-                                    tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, j * kBN, b + 1);
-                                if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, j * kBN, b + 1);
-                            }
+                        const long long nn = min(S.start(nb + 1), t_end) - x1;
+                        for (int j = 0; j < min(nn, 3LL); ++j) {
+                            const int r = kPaged ? 0 : j * kBN;
+                            const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(nb) * p.max_pages + j) : nb;
+                            for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, r, o);
+                            if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, r, o);
                         }
                     }
                     const int tile = static_cast<int>(x - P0);          // tile of the sequence
                     // dense: rows [64 tile, 64 tile + 64) of sequence b; paged: the tile's page
-                    // (read before the slot wait, so the load overlaps it)
+                    // (read a tile ahead, so the load overlaps the slot waits)
                     const int row0 = kPaged ? 0 : tile * kBN;
-                    const int outer = kPaged ? __ldg(pages + tile) : b;
+                    const int outer = outer_next;
+                    if (kPaged && x + 1 < x1) outer_next = __ldg(pages + tile + 1);
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
@@ -809,6 +815,7 @@ __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlen
 {
     __shared__ int warp_sum[32];
     __shared__ int carry;
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
@@ -1090,8 +1097,19 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
         e = cudaFuncSetAttribute(mla_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
-        mla_split_kernel<true><<<2 * C, kThreads, kSmemBytes, env.stream>>>(tkv, tkp, tqn, tqp, p);
-        e = cudaGetLastError();
+        // a programmatic dependent of the tile-table kernel (it waits for it
+        // before reading the table)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * C, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = env.stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, mla_split_kernel<true>, tkv, tkp, tqn, tqp, p);
     }
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
