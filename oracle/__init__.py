@@ -47,6 +47,8 @@ def _load():
             P, I, D, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_int64
             lib.oracle_attn_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I64, I]
             lib.oracle_attn_fwd.restype = I
+            lib.oracle_attn_fwd_masked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I, P, I64, I]
+            lib.oracle_attn_fwd_masked.restype = I
             lib.oracle_mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, P, I64, I]
             lib.oracle_mla_decode.restype = I
             lib.oracle_mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D, P, I64, I]
@@ -76,12 +78,14 @@ def _ptr(a: np.ndarray):
 
 
 def attn_fwd(Q, K, V, causal: bool, window: int, scale: float, rows=None,
-             return_probs: bool = False, threads: int | None = None):
+             return_probs: bool = False, threads: int | None = None, block_mask=None, block: int = 128):
     """Reference attention for bf16 Q [B,H,N_q,d], K/V [B,H_kv,N_kv,d].
 
     Returns (O, LSE[, P]) as float64 numpy arrays.  With ``rows`` (flat indices
     (b*H + h)*N_q + i) only those rows are computed: O is [len(rows), d] and LSE
-    [len(rows)].  Without it, O is [B,H,N_q,d] and LSE [B,H,N_q].
+    [len(rows)].  Without it, O is [B,H,N_q,d] and LSE [B,H,N_q].  ``block_mask``
+    (uint8 [B,H,ceil(N_q/block),ceil(N_kv/block)]) removes the keys of every
+    zero block from its query rows.
     """
     B, H, N_q, d = Q.shape
     _, H_kv, N_kv, _ = K.shape
@@ -95,9 +99,16 @@ def attn_fwd(Q, K, V, causal: bool, window: int, scale: float, rows=None,
     O = np.zeros((n, d), dtype=np.float64)
     LSE = np.zeros((n,), dtype=np.float64)
     P = np.zeros((n, N_kv), dtype=np.float64) if return_probs else None
-    rc = _load().oracle_attn_fwd(
+    mask = None
+    if block_mask is not None:
+        mask = np.ascontiguousarray(np.asarray(block_mask, dtype=np.uint8))
+        want = (B, H, -(-N_q // block), -(-N_kv // block))
+        if mask.shape != want:
+            raise ValueError(f"block_mask must have shape {want}, got {mask.shape}")
+    rc = _load().oracle_attn_fwd_masked(
         _ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(LSE), _ptr(P) if P is not None else None,
         B, H, H_kv, N_q, N_kv, d, int(bool(causal)), int(window), float(scale),
+        _ptr(mask) if mask is not None else None, int(block),
         _ptr(rows_arr) if rows_arr is not None else None, n, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")

@@ -35,7 +35,12 @@
  *    key j is visible iff i' - w <= j <= i' + w;
  *  - GQA maps query head h to key/value head h / (H / H_kv) (contiguous
  *    groups; the FlashMLA article's section 5.1 shows only kv_head_num = 1);
- *  - a row with no allowed key has O = 0 and LSE = -inf.
+ *  - a row with no allowed key has O = 0 and LSE = -inf;
+ *  - a block-sparse mask (the TileLang study notes' block-sparse variant:
+ *    attention computed only where a block-level mask is set) is a byte per
+ *    (batch, head, block of `blk` query rows, block of `blk` keys); a zero
+ *    byte removes those keys from those rows, on top of the causal / window
+ *    rules.
  *
  * Inputs are bf16 bit patterns (uint16), converted exactly to double.  All
  * arithmetic is fp64.  Rows are independent, so threads split the rows.
@@ -112,6 +117,8 @@ typedef struct {
     const int64_t *rows;   /* flat (b*H + h)*N_q + i, or NULL for all rows */
     int64_t n_rows;
     int n_threads, tid;
+    const uint8_t *block_mask;   /* [B][H][ceil(N_q/blk)][ceil(N_kv/blk)], or NULL */
+    int blk;
 } attn_job;
 
 static void attn_one_row(const attn_job *J, int64_t flat, int64_t out_idx, double *s)
@@ -126,9 +133,14 @@ static void attn_one_row(const attn_job *J, int64_t flat, int64_t out_idx, doubl
     const uint16_t *q = J->Q + ((b * J->H + h) * n_q + i) * d;
     const uint16_t *K = J->K + (b * J->H_kv + g) * n_kv * d;
     const uint16_t *V = J->V + (b * J->H_kv + g) * n_kv * d;
+    const uint8_t *mrow = NULL;
+    if (J->block_mask) {
+        const long nqb = (n_q + J->blk - 1) / J->blk, nkb = (n_kv + J->blk - 1) / J->blk;
+        mrow = J->block_mask + ((b * J->H + h) * nqb + i / J->blk) * nkb;
+    }
 
     for (long j = 0; j < n_kv; j++) {
-        if (!key_allowed(i, j, n_q, n_kv, J->causal, J->window)) {
+        if (!key_allowed(i, j, n_q, n_kv, J->causal, J->window) || (mrow && !mrow[j / J->blk])) {
             s[j] = -INFINITY;
             continue;
         }
@@ -176,10 +188,29 @@ static int run_threads(void *(*fn)(void *), void *jobs, size_t job_size, int n_t
  * receives the full probability row of each computed row ([n_rows, N_kv]).
  * Returns 0, or -1 on invalid arguments / allocation failure.
  */
+int oracle_attn_fwd_masked(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O, double *LSE,
+                           double *P, int B, int H, int H_kv, int N_q, int N_kv, int d, int causal,
+                           int window, double scale, const uint8_t *block_mask, int blk,
+                           const int64_t *rows, int64_t n_rows, int n_threads);
+
 int oracle_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O, double *LSE,
                     double *P, int B, int H, int H_kv, int N_q, int N_kv, int d, int causal,
                     int window, double scale, const int64_t *rows, int64_t n_rows, int n_threads)
 {
+    return oracle_attn_fwd_masked(Q, K, V, O, LSE, P, B, H, H_kv, N_q, N_kv, d, causal, window, scale,
+                                  NULL, 1, rows, n_rows, n_threads);
+}
+
+/*
+ * oracle_attn_fwd_masked: oracle_attn_fwd with an optional block-sparse mask
+ * (NULL: none) of blk x blk (query rows x keys) blocks.
+ */
+int oracle_attn_fwd_masked(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O, double *LSE,
+                           double *P, int B, int H, int H_kv, int N_q, int N_kv, int d, int causal,
+                           int window, double scale, const uint8_t *block_mask, int blk,
+                           const int64_t *rows, int64_t n_rows, int n_threads)
+{
+    if (blk < 1) return -1;
     if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv || N_q < 0 || N_kv < 0 || d <= 0) return -1;
     int64_t total = (int64_t)B * H * N_q;
     if (!rows) n_rows = total;
@@ -193,7 +224,7 @@ int oracle_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, dou
     if (!jobs) return -1;
     for (int t = 0; t < n_threads; t++) {
         attn_job j = {Q, K, V, O, LSE, P, B, H, H_kv, N_q, N_kv, d, causal, window,
-                      scale, rows, n_rows, n_threads, t};
+                      scale, rows, n_rows, n_threads, t, block_mask, blk};
         jobs[t] = j;
     }
     int rc = run_threads(attn_worker, jobs, sizeof(attn_job), n_threads);

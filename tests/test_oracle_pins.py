@@ -296,6 +296,55 @@ def test_mla_rows_subset():
     np.testing.assert_array_equal(Ls, LSE.reshape(-1)[[1, 4]])
 
 
+def _expand_block_mask(mask, n_q, n_kv, block):
+    m = mask.bool().repeat_interleave(block, 2).repeat_interleave(block, 3)
+    return m[:, :, :n_q, :n_kv]
+
+
+def test_block_mask_all_ones_is_dense():
+    Q, K, V = wl.random_prefill(2, 4, 2, 70, 90, 16, seed=50)
+    ones = torch.ones(2, 4, 3, 3, dtype=torch.uint8)
+    for causal in (False, True):
+        O1, L1 = oracle.attn_fwd(Q, K, V, causal, 0, 0.3)
+        O2, L2 = oracle.attn_fwd(Q, K, V, causal, 0, 0.3, block_mask=ones, block=32)
+        np.testing.assert_array_equal(O1, O2)
+        np.testing.assert_array_equal(L1, L2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_matches_sdpa_with_expanded_mask(causal):
+    n_q, n_kv, blk = 40, 52, 8
+    Q, K, V = wl.random_prefill(2, 4, 2, n_q, n_kv, 16, seed=51)
+    mask = wl.random_block_mask(2, 4, n_q, n_kv, 0.5, seed=52, block=blk)
+    mask[1, 2, 3] = 0                              # query rows 24..31 of (1, 2) see no key
+    O, LSE = oracle.attn_fwd(Q, K, V, causal, 0, 0.25, block_mask=mask, block=blk)
+    allowed = _expand_block_mask(mask, n_q, n_kv, blk)
+    if causal:
+        i = torch.arange(n_q)[:, None] + (n_kv - n_q)
+        allowed = allowed & (torch.arange(n_kv)[None, :] <= i)
+    Kr, Vr = (f64(x).repeat_interleave(2, dim=1) for x in (K, V))
+    s = (f64(Q) @ Kr.transpose(-1, -2)) * 0.25
+    s = s.masked_fill(~allowed, -math.inf)
+    np.testing.assert_allclose(LSE, torch.logsumexp(s, -1).numpy(), atol=1e-12, rtol=0)
+    rows = allowed.any(-1)
+    p = torch.softmax(s.masked_fill(~rows[..., None], 0.0), -1) * rows[..., None]
+    np.testing.assert_allclose(O, (p @ Vr).numpy(), atol=1e-12, rtol=0)
+    assert (~rows).any() and (O[~rows.numpy()] == 0).all() and np.isneginf(LSE[~rows.numpy()]).all()
+
+
+def test_block_mask_uniform_scores_closed_form():
+    n_q, n_kv, blk = 12, 16, 4
+    _, K, V = wl.random_prefill(1, 1, 1, n_q, n_kv, 8, seed=53)
+    Q = torch.zeros(1, 1, n_q, 8, dtype=torch.bfloat16)
+    mask = torch.tensor([[[[1, 0, 1, 0], [0, 0, 0, 1], [1, 1, 1, 1]]]], dtype=torch.uint8)
+    O, LSE = oracle.attn_fwd(Q, K, V, False, 0, 0.7, block_mask=mask, block=blk)
+    v = f64(V[0, 0]).numpy()
+    for i in range(n_q):
+        keys = [j for j in range(n_kv) if mask[0, 0, i // blk, j // blk]]
+        np.testing.assert_allclose(O[0, 0, i], v[keys].mean(0), atol=1e-12)
+        assert abs(LSE[0, 0, i] - math.log(len(keys))) < 1e-12
+
+
 def _dense_as_paged(KV, Kp, page):
     """The dense [B,N,d] caches as pages in order: sequence b owns pages b*N/page ..."""
     B, N, d_c = KV.shape

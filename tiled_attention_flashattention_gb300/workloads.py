@@ -153,3 +153,11 @@ def random_mla_paged(H, seqlens, d_c=512, d_r=64, page=64, spare_pages=3, seed=0
         table[b, :n] = perm[k:k + n].to(torch.int32)
         k += n
     return Qn, Qp, KV, Kp, table, torch.tensor(lens, dtype=torch.int32)
+
+
+def random_block_mask(B, H, N_q, N_kv, density, seed, block=128):
+    """uint8 [B,H,ceil(N_q/block),ceil(N_kv/block)]: each block set with
+    probability `density` (torch CPU generator)."""
+    g = _gen(seed)
+    shape = (B, H, -(-N_q // block), -(-N_kv // block))
+    return (torch.rand(*shape, generator=g) < density).to(torch.uint8)
