@@ -305,6 +305,56 @@ def paged_decode_workload(gb, dev, peaks, flush, reps=10):
             "ms": t * 1e3, "total_keys": int(sum(lens)), "algorithmic_bytes": by}
 
 
+def sparse_pairs(mask, N_q: int, N_kv: int, causal: bool, window: int, block: int = 128) -> int:
+    """(query, key) pairs that both the element mask and the block mask keep,
+    summed over (batch, head).  mask: uint8 [B,H,ceil(N_q/block),ceil(N_kv/block)]."""
+    i = np.arange(N_q, dtype=np.int64)
+    lo, hi = key_bounds(i, N_q, N_kv, causal, window)
+    kb = np.arange(-(-N_kv // block), dtype=np.int64)
+    k0 = kb * block
+    k1 = np.minimum(k0 + block, N_kv) - 1
+    # allowed keys of row i inside key block kb: |[lo_i, hi_i] ∩ [k0, k1]|
+    per = np.maximum(0, np.minimum(hi[:, None], k1[None, :]) - np.maximum(lo[:, None], k0[None, :]) + 1)
+    qb = -(-N_q // block)
+    per = np.pad(per, ((0, qb * block - N_q), (0, 0)))
+    block_pairs = per.reshape(qb, block, -1).sum(1)                # [QB, KB]
+    m = mask.numpy().astype(np.int64)                              # [B,H,QB,KB]
+    return int((m * block_pairs[None, None]).sum())
+
+
+def sparse_prefill_workload(gb, dev, peaks, flush, reps=10):
+    """Kernel-only TFLOP/s of attn_fwd_sparse on the 8k causal GQA inputs with a
+    seeded 25 %-density block mask (L2 flushed before each timed launch).  The
+    algorithmic work counts only pairs inside active blocks that the causal
+    mask keeps."""
+    c = wl.WORKLOADS["gqa_causal_b2_h32_hkv8_n8192_d128"]
+    mask_h = wl.random_block_mask(c.B, c.H, c.N_q, c.N_kv, 0.25, seed=wl.SEED_BASE + 6)
+    Q, K, V = (x.to(dev) for x in wl.prefill_inputs(c))
+    mask = mask_h.to(dev)
+    O = torch.empty_like(Q)
+    L = torch.empty(c.B, c.H, c.N_q, dtype=torch.float32, device=dev)
+    call = lambda: gb.attn_fwd_sparse(Q, K, V, mask, causal=True, scale=c.softmax_scale(), O=O, LSE=L)
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream(dev)
+    total = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    gb.check()
+    t = total / reps
+    flops = 4.0 * c.d * sparse_pairs(mask_h, c.N_q, c.N_kv, True, 0)
+    tf = flops / t / 1e12
+    return {"workload": "gqa_causal_sparse25_b2_h32_hkv8_n8192_d128", "tflops": tf,
+            "frac_bf16_peak": tf / peaks["bf16_tflops"], "ms": t * 1e3,
+            "active_blocks": int(mask_h.sum()), "algorithmic_flops": flops}
+
+
 def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
     """Kernel-only TFLOP/s of the other prefill workloads (inputs resident,
     L2 flushed before each timed launch, CUDA events around the launch)."""
@@ -485,6 +535,7 @@ def run_ours(args, rank, world, local):
     if not args.no_extra:
         line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
         line["decode_paged"] = paged_decode_workload(gb, dev, peaks, flush)
+        line["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks, flush)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)

@@ -85,6 +85,24 @@ int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
              int causal, int window, float scale, void *stream);
 
 /*
+ * attn_fwd_sparse -- attn_fwd with a block-sparse mask (the study notes'
+ * block-sparse variant: attention is computed only in the blocks a
+ * block-level mask selects).
+ *
+ * block_mask: uint8 [B, H, ceil(N_q / 128), ceil(N_kv / 128)] on the device,
+ * one byte per (batch, query head, block of 128 query rows, block of 128
+ * keys); a zero byte removes those keys from those rows, on top of the
+ * causal / window rules of attn_fwd (whose other arguments it shares).  A row
+ * left without keys gets O = 0, LSE = -inf.  Skipped blocks are neither
+ * loaded nor computed.  The mask must stay unchanged until the call has run.
+ * Errors as attn_fwd (a null block_mask with N_kv > 0 is
+ * GBATTN_ERR_INVALID_ARG).
+ */
+int attn_fwd_sparse(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                    const unsigned char *block_mask, int B, int H, int H_kv, int N_q, int N_kv, int d,
+                    int causal, int window, float scale, void *stream);
+
+/*
  * mla_decode_workspace_bytes -- size of the scratch buffer mla_decode needs
  * for the given shape on the current device (it depends on the device's SM
  * count).  Returns 0 for an invalid shape.

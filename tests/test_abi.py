@@ -60,6 +60,19 @@ def test_attn_fwd_argument_errors(lib):
     assert b"16-byte" in lib.gbattn_last_error() or b"aligned" in lib.gbattn_last_error()
 
 
+def test_attn_fwd_sparse_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def sparse(mask=16, d=64, causal=0, H=2, H_kv=2, K=16):
+        return lib.attn_fwd_sparse(vp(16), vp(K), vp(16), vp(16), vp(16), vp(mask), 1, H, H_kv, 8, 8, d, causal, 0,
+                                   ctypes.c_float(0.125), None)
+    assert sparse(mask=0) == 1                     # null mask with keys present
+    assert sparse(d=96) == 2
+    assert sparse(causal=3) == 1
+    assert sparse(H=3, H_kv=2) == 1
+    assert sparse(K=24) == 3
+
+
 def test_mla_decode_argument_errors(lib):
     vp = ctypes.c_void_p
 

@@ -51,6 +51,8 @@ def load_library():
         P, I, F, SZ, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd.restype = I
+        lib.attn_fwd_sparse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_sparse.restype = I
         lib.mla_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.mla_decode_workspace_bytes.restype = SZ
         lib.mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
@@ -131,6 +133,34 @@ def attn_fwd(Q, K, V, causal: bool = False, window: int = 0, scale: float | None
     _need(LSE, "LSE", torch.float32, (B, H, N_q))
     rc = lib.attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, H_kv, N_q, N_kv, d,
                       int(bool(causal)), int(window), float(scale), ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def attn_fwd_sparse(Q, K, V, block_mask, causal: bool = False, window: int = 0, scale: float | None = None,
+                    O=None, LSE=None, stream=None):
+    """attn_fwd with a block-sparse mask: block_mask uint8 [B,H,ceil(N_q/128),ceil(N_kv/128)]
+    (CUDA); a zero byte removes those 128 keys from those 128 query rows (on top
+    of causal / window).  Skipped blocks are neither loaded nor computed."""
+    lib = load_library()
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("Q, K, V must be 4-D [B, H, N, d]")
+    B, H, N_q, d = Q.shape
+    _, H_kv, N_kv, _ = K.shape
+    _need(Q, "Q", torch.bfloat16, None)
+    _need(K, "K", torch.bfloat16, (B, H_kv, N_kv, d))
+    _need(V, "V", torch.bfloat16, (B, H_kv, N_kv, d))
+    _need(block_mask, "block_mask", torch.uint8, (B, H, -(-N_q // 128), -(-N_kv // 128)))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty((B, H, N_q, d), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None:
+        LSE = torch.empty((B, H, N_q), dtype=torch.float32, device=Q.device)
+    _need(O, "O", torch.bfloat16, (B, H, N_q, d))
+    _need(LSE, "LSE", torch.float32, (B, H, N_q))
+    rc = lib.attn_fwd_sparse(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(block_mask), B, H, H_kv, N_q, N_kv,
+                             d, int(bool(causal)), int(window), float(scale), ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return O, LSE
 

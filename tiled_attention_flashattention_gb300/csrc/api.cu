@@ -122,35 +122,53 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
 
 using namespace gbattn;
 
-extern "C" int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
-                        int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
-                        void *stream)
+static int attn_fwd_common(const char *name, const void *Q, const void *K, const void *V, void *O, float *LSE,
+                           const uint8_t *block_mask, bool sparse, int B, int H, int H_kv, int N_q, int N_kv,
+                           int d, int causal, int window, float scale, void *stream)
 {
     g_err.clear();
+    const std::string n(name);
     if (B < 0 || H < 1 || H_kv < 1 || N_q < 0 || N_kv < 0)
-        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: need B >= 0, H >= 1, H_kv >= 1, N_q >= 0, N_kv >= 0");
-    if (H % H_kv != 0) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: H must be a multiple of H_kv");
-    if (causal != 0 && causal != 1) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
-    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
-    if (d != 64 && d != 128) return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: d must be 64 or 128");
+        return fail(GBATTN_ERR_INVALID_ARG, n + ": need B >= 0, H >= 1, H_kv >= 1, N_q >= 0, N_kv >= 0");
+    if (H % H_kv != 0) return fail(GBATTN_ERR_INVALID_ARG, n + ": H must be a multiple of H_kv");
+    if (causal != 0 && causal != 1) return fail(GBATTN_ERR_INVALID_ARG, n + ": causal must be 0 or 1");
+    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, n + ": scale must be finite and > 0");
+    if (d != 64 && d != 128) return fail(GBATTN_ERR_UNSUPPORTED, n + ": d must be 64 or 128");
     if (static_cast<long long>(B) * H * N_q > (1LL << 40) || static_cast<long long>(N_q) * d > (1LL << 31) ||
         static_cast<long long>(N_kv) * d > (1LL << 31))
-        return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd: problem too large");
+        return fail(GBATTN_ERR_UNSUPPORTED, n + ": problem too large");
     const bool work = static_cast<long long>(B) * H * N_q > 0;
-    if (work && (!Q || !O || !LSE || (N_kv > 0 && (!K || !V))))
-        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd: null tensor pointer");
+    if (work && (!Q || !O || !LSE || (N_kv > 0 && (!K || !V)) || (sparse && N_kv > 0 && !block_mask)))
+        return fail(GBATTN_ERR_INVALID_ARG, n + ": null tensor pointer");
     if (work && (!aligned16(Q) || !aligned16(O) || (N_kv > 0 && (!aligned16(K) || !aligned16(V)))))
-        return fail(GBATTN_ERR_ALIGNMENT, "attn_fwd: Q, K, V and O must be 16-byte aligned");
+        return fail(GBATTN_ERR_ALIGNMENT, n + ": Q, K, V and O must be 16-byte aligned");
     if (work && (reinterpret_cast<uintptr_t>(LSE) & 3u))
-        return fail(GBATTN_ERR_ALIGNMENT, "attn_fwd: LSE must be 4-byte aligned");
+        return fail(GBATTN_ERR_ALIGNMENT, n + ": LSE must be 4-byte aligned");
     LaunchEnv env;
     int rc = get_env(env, stream);
     if (rc != GBATTN_OK) return rc;
     if (!work) return GBATTN_OK;
     std::string err;
-    rc = launch_attn_fwd(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, causal, window, scale, env, err);
+    rc = launch_attn_fwd(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, causal, window, scale,
+                         sparse ? block_mask : nullptr, env, err);
     if (rc != GBATTN_OK) g_err = err;
     return rc;
+}
+
+extern "C" int attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                        int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
+                        void *stream)
+{
+    return attn_fwd_common("attn_fwd", Q, K, V, O, LSE, nullptr, false, B, H, H_kv, N_q, N_kv, d, causal, window,
+                           scale, stream);
+}
+
+extern "C" int attn_fwd_sparse(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                               const unsigned char *block_mask, int B, int H, int H_kv, int N_q, int N_kv, int d,
+                               int causal, int window, float scale, void *stream)
+{
+    return attn_fwd_common("attn_fwd_sparse", Q, K, V, O, LSE, block_mask, true, B, H, H_kv, N_q, N_kv, d, causal,
+                           window, scale, stream);
 }
 
 extern "C" size_t mla_decode_workspace_bytes(int B, int H, int N_kv, int d_c)

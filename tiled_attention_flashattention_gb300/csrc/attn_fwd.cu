@@ -72,6 +72,7 @@ struct Ctl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int sp_lo[2], sp_hi[2];     // block-sparse form: first / last + 1 active key block of each Q tile
 };
 
 template <int D>
@@ -89,6 +90,10 @@ struct Params {
     int lo_pad, hi_pad;
     int group;          // H / H_kv
     int n_qblk;         // ceil(N_q / 256)
+    // Block-sparse form only: a byte per (b, h, 128-row query block, 128-key
+    // block), [B][H][ceil(N_q/128)][ceil(N_kv/128)]; 0 skips the block.
+    const uint8_t *block_mask;
+    int mask_qb, mask_kb;
     float c;            // scale * log2(e)
     int inject;         // 1: the producer never loads the Q tiles (tests the bounded waits)
     int *status;
@@ -109,7 +114,7 @@ __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
     return {static_cast<int>(key_lo / kBN), static_cast<int>((key_hi + kBN - 1) / kBN)};
 }
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -148,6 +153,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (lo > hi) lo = hi = 0;
+    // Block-sparse form: the mask row of each Q tile (its 128-row query block).
+    const uint8_t *mrow[2] = {nullptr, nullptr};
+    if constexpr (kSparse) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (r0[t] < p.N_q)
+                mrow[t] = p.block_mask + (static_cast<size_t>(bh) * p.mask_qb + r0[t] / kBM) * p.mask_kb;
+    }
+    auto in_rng = [&](int t, int j) { return j >= rng[t].lo && j < rng[t].hi; };
+    // does Q tile t compute key block j?
+    auto act = [&](int t, int j) -> bool {
+        if constexpr (kSparse)
+            return in_rng(t, j) && __ldg(mrow[t] + j) != 0;
+        else
+            return in_rng(t, j);
+    };
+    // the next key block after j that some Q tile computes (hi if none)
+    auto next_any = [&](int j) -> int {
+        int k = j + 1;
+        if constexpr (kSparse)
+            while (k < hi && !act(0, k) && !act(1, k)) ++k;
+        return k;
+    };
 
     // ---- setup
     if (threadIdx.x == 0) {
@@ -170,10 +198,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before_sync();
     }
+    if constexpr (kSparse) {
+        if (warp == 2) {
+            // first and last active key block of each Q tile, one scan of the mask
+            for (int t = 0; t < 2; ++t) {
+                int f = 0x7fffffff, l = -1;
+                for (int j = rng[t].lo + lane; j < rng[t].hi; j += 32)
+                    if (__ldg(mrow[t] + j)) {
+                        f = min(f, j);
+                        l = max(l, j);
+                    }
+                f = __reduce_min_sync(0xffffffffu, f);
+                l = __reduce_max_sync(0xffffffffu, l);
+                if (lane == 0) {
+                    c.sp_lo[t] = f;
+                    c.sp_hi[t] = l + 1;
+                }
+            }
+        }
+    }
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tbase = c.tmem_base;
     const WaitCtl ctl{&c.abort, p.status, p.timeout_ns};
+    int first = lo;          // the first key block some Q tile computes
+    if constexpr (kSparse) {
+        first = hi;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            has[t] = has[t] && c.sp_hi[t] > c.sp_lo[t];   // a tile with no active block writes O = 0
+            if (has[t]) first = min(first, c.sp_lo[t]);
+        }
+    }
 
     if (warp == 0) {
         // =================== TMA producer ===================
@@ -196,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             int it = 0;
-            for (int j = lo; j < hi && ok; ++j) {
+            for (int j = first; j < hi && ok; j = next_any(j)) {
                 for (int kv = 0; kv < 2; ++kv) {
                     const int slot = it % C::kSlots;
                     const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
@@ -249,60 +305,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_ts(tbase + C::col_o(t), tbase + C::col_s(t) + k * 8, desc_advance(bd, k * 2048), idPV, 1u);
                 started[t] = true;
             };
-            auto in_rng = [&](int t, int j) { return j >= rng[t].lo && j < rng[t].hi; };
-
             bool ok = true;
-            if (hi > lo) ok = mbar_wait(&c.q_full, 0, ctl);
             int it = 0;
             uint32_t pcount[2] = {0, 0};
-            if (ok && hi > lo) {
+            if (first < hi) ok = mbar_wait(&c.q_full, 0, ctl);
+            if (ok && first < hi) {
                 const int slotK = 0;
                 ok = mbar_wait(&c.full[slotK], 0, ctl);
                 ++it;
                 if (ok) {
                     tc_fence_after_sync();
                     for (int t = 0; t < 2; ++t)
-                        if (in_rng(t, lo)) {
+                        if (act(t, first)) {
                             issue_S(t, slotK);
                             umma_commit(&c.s_full[t]);
                         }
                     umma_commit(&c.empty[slotK]);
                 }
             }
-            for (int j = lo; j < hi && ok; ++j) {
+            // Key blocks in the producer's order (every block some Q tile computes):
+            // PV of block j for tile 0, S of the next block for tile 0, PV of j for
+            // tile 1, S of the next block for tile 1.
+            for (int j = first; j < hi && ok;) {
                 const int slotV = it % C::kSlots;
                 if (!(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                     break;
                 ++it;
-                if (in_rng(0, j)) {
+                if (act(0, j)) {
                     if (!(ok = mbar_wait(&c.p_full[0], pcount[0]++ & 1u, ctl))) break;
                     tc_fence_after_sync();
                     issue_PV(0, slotV);
                 }
+                const int jn = next_any(j);
                 int slotK = -1;
-                if (j + 1 < hi) {
+                if (jn < hi) {
                     slotK = it % C::kSlots;
                     if (!(ok = mbar_wait(&c.full[slotK], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                         break;
                     ++it;
-                    if (in_rng(0, j + 1)) {
+                    if (act(0, jn)) {
                         issue_S(0, slotK);
                         umma_commit(&c.s_full[0]);
                     }
                 }
-                if (in_rng(1, j)) {
+                if (act(1, j)) {
                     if (!(ok = mbar_wait(&c.p_full[1], pcount[1]++ & 1u, ctl))) break;
                     tc_fence_after_sync();
                     issue_PV(1, slotV);
                 }
                 umma_commit(&c.empty[slotV]);
                 if (slotK >= 0) {
-                    if (in_rng(1, j + 1)) {
+                    if (act(1, jn)) {
                         issue_S(1, slotK);
                         umma_commit(&c.s_full[1]);
                     }
                     umma_commit(&c.empty[slotK]);
                 }
+                j = jn;
             }
             for (int t = 0; t < 2; ++t)
                 if (has[t]) umma_commit(&c.o_final[t]);
@@ -335,6 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int n = 0;
         for (int j = rng[t].lo; j < rng[t].hi && ok; ++j, ++n) {
+            if constexpr (kSparse) {
+                if (!act(t, j)) {              // a block this tile skips (warp-uniform)
+                    --n;
+                    continue;
+                }
+            }
             // tcgen05.ld/st below are warp-collective: keep the outcome warp-uniform.
             ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[t], static_cast<uint32_t>(n) & 1u, ctl));
             if (!ok) break;
@@ -454,14 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kSparse>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
            const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
     static bool configured = false;   // per process; attribute is per function
     const size_t smem = smem_bytes<D>();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) {
@@ -470,7 +535,7 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
         }
         configured = true;
     }
-    attn_fwd_kernel<D><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
+    attn_fwd_kernel<D, kSparse><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
@@ -493,7 +558,7 @@ __global__ void fill_empty_kernel(__nv_bfloat16 *O, float *LSE, size_t rows, int
 
 int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                     int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
-                    const LaunchEnv &env, std::string &err)
+                    const uint8_t *block_mask, const LaunchEnv &env, std::string &err)
 {
     if (N_q == 0 || B == 0) return 0;
     if (N_kv == 0) {
@@ -530,6 +595,9 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         p.lo_pad = window > 0 ? window : kNoPad;
     }
     p.group = H / H_kv;
+    p.block_mask = block_mask;
+    p.mask_qb = (N_q + kBM - 1) / kBM;
+    p.mask_kb = (N_kv + kBN - 1) / kBN;
     p.n_qblk = (N_q + kQTiles * kBM - 1) / (kQTiles * kBM);
     p.c = scale * 1.4426950408889634f;
     p.inject = env.inject;
@@ -540,8 +608,12 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         err = "attn_fwd: problem too large for one launch";
         return 2;
     }
-    if (d == 128) return launch<128>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
-    return launch<64>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    if (block_mask) {
+        if (d == 128) return launch<128, true>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+        return launch<64, true>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    }
+    if (d == 128) return launch<128, false>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    return launch<64, false>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
 }
 
 }  // namespace gbattn

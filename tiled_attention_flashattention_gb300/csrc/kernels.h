@@ -28,9 +28,10 @@ struct LaunchEnv {
 
 // Prefill attention forward (attn_fwd).  Pointers are device pointers, already
 // validated by the caller; returns a gbattn_status value.
+// block_mask: nullptr, or the block-sparse mask of attn_fwd_sparse (device).
 int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
                     int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
-                    const LaunchEnv &env, std::string &err);
+                    const uint8_t *block_mask, const LaunchEnv &env, std::string &err);
 
 // MLA decode (mla_decode).
 size_t mla_workspace_bytes(int B, int H, int N_kv, int d_c, int num_sms);
