@@ -51,7 +51,7 @@ def _load():
             lib.oracle_attn_fwd_masked.restype = I
             lib.oracle_mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, P, I64, I]
             lib.oracle_mla_decode.restype = I
-            lib.oracle_mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D, P, I64, I]
+            lib.oracle_mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I64, I]
             lib.oracle_mla_decode_paged.restype = I
             _lib = lib
     return _lib
@@ -150,12 +150,19 @@ def mla_decode(Q_nope, Q_pe, KV_latent, K_pe, scale: float, rows=None, threads: 
 
 def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, scale: float, rows=None,
                      threads: int | None = None):
-    """Reference MLA decode over a paged KV cache: Q_nope [B,H,d_c], Q_pe [B,H,d_r]
-    (bf16), KV_cache [num_pages,page,d_c], K_pe_cache [num_pages,page,d_r] (bf16),
-    block_table [B,max_pages] and seqlens [B] (int32).  Key j of sequence b is row
-    j % page of page block_table[b, j // page].  Returns (O [B,H,d_c], LSE [B,H])
-    float64, or the listed flat rows b*H + h only."""
-    B, H, d_c = Q_nope.shape
+    """Reference MLA decode over a paged KV cache: Q_nope [B,H,d_c] or [B,s_q,H,d_c],
+    Q_pe [B,(s_q,)H,d_r] (bf16), KV_cache [num_pages,page,d_c], K_pe_cache
+    [num_pages,page,d_r] (bf16), block_table [B,max_pages] and seqlens [B] (int32).
+    Key j of sequence b is row j % page of page block_table[b, j // page]; query
+    token t of s_q sees keys j < seqlens[b] - (s_q - 1 - t).  Returns (O, LSE)
+    float64 shaped like Q_nope (last dim d_c) and Q_nope without its last dim, or
+    the listed flat rows (b*s_q + t)*H + h only."""
+    multi = Q_nope.dim() == 4
+    if multi:
+        B, s_q, H, d_c = Q_nope.shape
+    else:
+        B, H, d_c = Q_nope.shape
+        s_q = 1
     d_r = Q_pe.shape[-1]
     num_pages, page, _ = KV_cache.shape
     max_pages = block_table.shape[1]
@@ -168,15 +175,17 @@ def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, s
     else:
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = rows_arr.shape[0]
+    if rows is None:
+        n = B * s_q * H
     O = np.zeros((n, d_c), dtype=np.float64)
     LSE = np.zeros((n,), dtype=np.float64)
     rc = _load().oracle_mla_decode_paged(
-        _ptr(qn), _ptr(qp), _ptr(kv), _ptr(kp), _ptr(table), _ptr(lens), _ptr(O), _ptr(LSE), B, H,
+        _ptr(qn), _ptr(qp), _ptr(kv), _ptr(kp), _ptr(table), _ptr(lens), _ptr(O), _ptr(LSE), B, s_q, H,
         num_pages, max_pages, page, d_c, d_r, float(scale),
         _ptr(rows_arr) if rows_arr is not None else None, n, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_mla_decode_paged rejected its arguments")
     if rows is None:
-        O = O.reshape(B, H, d_c)
-        LSE = LSE.reshape(B, H)
+        O = O.reshape(B, s_q, H, d_c) if multi else O.reshape(B, H, d_c)
+        LSE = LSE.reshape(B, s_q, H) if multi else LSE.reshape(B, H)
     return O, LSE

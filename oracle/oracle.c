@@ -304,14 +304,16 @@ int oracle_mla_decode(const uint16_t *Q_nope, const uint16_t *Q_pe, const uint16
 /* per sequence).  Key j < seqlens[b] of sequence b is row j % page of page   */
 /* block_table[b * max_pages + j / page] of the caches                        */
 /*   KV_cache [num_pages][page][d_c],  K_pe_cache [num_pages][page][d_r];     */
-/* otherwise the same definition as oracle_mla_decode.  A sequence of length  */
-/* 0 has O = 0 and LSE = -inf.                                                */
+/* otherwise the same definition as oracle_mla_decode.  With s_q query tokens */
+/* per sequence (Q [B][s_q][H][d], O [B][s_q][H][d_c]), the tokens are the    */
+/* last s_q positions of the sequence and attend causally: token t sees keys  */
+/* j < seqlens[b] - (s_q - 1 - t).  A row with no key has O = 0, LSE = -inf.  */
 
 typedef struct {
     const uint16_t *Qn, *Qp, *KV, *Kp;
     const int32_t *table, *seqlens;
     double *O, *LSE;
-    int B, H, max_pages, page, d_c, d_r;
+    int B, s_q, H, max_pages, page, d_c, d_r;
     double scale;
     const int64_t *rows;   /* flat b*H + h, or NULL */
     int64_t n_rows;
@@ -333,9 +335,11 @@ static void *mla_paged_worker(void *arg)
         return (void *)1;
     }
     for (int64_t k = J->tid; k < J->n_rows; k += J->n_threads) {
-        int64_t flat = J->rows ? J->rows[k] : k;
-        long b = (long)(flat / J->H), h = (long)(flat % J->H);
-        const long n = J->seqlens[b];
+        int64_t flat = J->rows ? J->rows[k] : k;   /* (b * s_q + t) * H + h */
+        long bt = (long)(flat / J->H), h = (long)(flat % J->H);
+        long b = bt / J->s_q, tok = bt % J->s_q;
+        long n = (long)J->seqlens[b] - (J->s_q - 1 - tok);
+        if (n < 0) n = 0;
         /* gather this sequence's key rows in order */
         for (long j = 0; j < n; j++) {
             const long pg = J->table[b * J->max_pages + j / J->page];
@@ -343,8 +347,8 @@ static void *mla_paged_worker(void *arg)
             memcpy(kv + j * dc, J->KV + r * dc, sizeof(uint16_t) * dc);
             memcpy(kp + j * dr, J->Kp + r * dr, sizeof(uint16_t) * dr);
         }
-        const uint16_t *qn = J->Qn + (b * J->H + h) * dc;
-        const uint16_t *qp = J->Qp + (b * J->H + h) * dr;
+        const uint16_t *qn = J->Qn + (bt * J->H + h) * dc;
+        const uint16_t *qp = J->Qp + (bt * J->H + h) * dr;
         for (long j = 0; j < n; j++) {
             double nope = 0.0, rope = 0.0;
             for (int c = 0; c < dc; c++) nope += bf16_to_f64(qn[c]) * bf16_to_f64(kv[j * dc + c]);
@@ -361,10 +365,11 @@ static void *mla_paged_worker(void *arg)
 
 int oracle_mla_decode_paged(const uint16_t *Q_nope, const uint16_t *Q_pe, const uint16_t *KV_cache,
                             const uint16_t *K_pe_cache, const int32_t *block_table, const int32_t *seqlens,
-                            double *O, double *LSE, int B, int H, int num_pages, int max_pages, int page,
+                            double *O, double *LSE, int B, int s_q, int H, int num_pages, int max_pages, int page,
                             int d_c, int d_r, double scale, const int64_t *rows, int64_t n_rows, int n_threads)
 {
-    if (B < 0 || H <= 0 || num_pages < 0 || max_pages < 0 || page <= 0 || d_c <= 0 || d_r < 0) return -1;
+    if (B < 0 || s_q < 1 || H <= 0 || num_pages < 0 || max_pages < 0 || page <= 0 || d_c <= 0 || d_r < 0)
+        return -1;
     for (int b = 0; b < B; b++) {
         if (seqlens[b] < 0 || (long)seqlens[b] > (long)max_pages * page) return -1;
         for (long j = 0; j < seqlens[b]; j += page) {
@@ -372,7 +377,7 @@ int oracle_mla_decode_paged(const uint16_t *Q_nope, const uint16_t *Q_pe, const 
             if (pg < 0 || pg >= num_pages) return -1;
         }
     }
-    int64_t total = (int64_t)B * H;
+    int64_t total = (int64_t)B * s_q * H;
     if (!rows) n_rows = total;
     if (n_rows == 0) return 0;
     for (int64_t k = 0; rows && k < n_rows; k++)
@@ -383,7 +388,7 @@ int oracle_mla_decode_paged(const uint16_t *Q_nope, const uint16_t *Q_pe, const 
     mla_paged_job *jobs = (mla_paged_job *)malloc(sizeof(mla_paged_job) * n_threads);
     if (!jobs) return -1;
     for (int t = 0; t < n_threads; t++) {
-        mla_paged_job j = {Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, O, LSE, B, H,
+        mla_paged_job j = {Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, O, LSE, B, s_q, H,
                            max_pages, page, d_c, d_r, scale, rows, n_rows, n_threads, t};
         jobs[t] = j;
     }

@@ -395,6 +395,20 @@ def test_mla_paged_empty_sequence():
     assert np.isfinite(L[1]).all()
 
 
+def test_mla_paged_query_tokens_are_truncated_single_token_calls():
+    # s_q query tokens are the last s_q positions: token t sees keys < len - (s_q - 1 - t)
+    lens, s_q = [5, 70, 130, 1], 3
+    Qn, Qp, KV, Kp, table, L = wl.random_mla_paged(4, lens, d_c=64, d_r=16, page=64, seed=35, s_q=s_q)
+    O, LSE = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, 0.1)
+    assert O.shape == (4, s_q, 4, 64) and LSE.shape == (4, s_q, 4)
+    for t in range(s_q):
+        short = torch.clamp(L - (s_q - 1 - t), min=0)
+        Ot, Lt = oracle.mla_decode_paged(Qn[:, t].contiguous(), Qp[:, t].contiguous(), KV, Kp, table, short, 0.1)
+        np.testing.assert_array_equal(O[:, t], Ot)
+        np.testing.assert_array_equal(LSE[:, t], Lt)
+    assert (O[3, 0] == 0).all() and np.isneginf(LSE[3, :2]).all()    # length 1: tokens 0 and 1 see nothing
+
+
 def test_mla_paged_rejects_bad_tables():
     Qn, Qp, KV, Kp, table, lens = wl.random_mla_paged(2, [70, 10], d_c=64, d_r=16, page=64, seed=34)
     with pytest.raises(ValueError):

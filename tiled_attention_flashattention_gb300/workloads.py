@@ -129,8 +129,9 @@ def random_mla(B, H, N_kv, d_c, d_r, seed):
                  for s in shapes)
 
 
-def random_mla_paged(H, seqlens, d_c=512, d_r=64, page=64, spare_pages=3, seed=0):
-    """Paged MLA decode inputs: Q_nope [B,H,d_c], Q_pe [B,H,d_r] (bf16),
+def random_mla_paged(H, seqlens, d_c=512, d_r=64, page=64, spare_pages=3, seed=0, s_q=1):
+    """Paged MLA decode inputs: Q_nope [B,H,d_c], Q_pe [B,H,d_r] (bf16; with
+    s_q > 1 query tokens per sequence [B,s_q,H,d_c] and [B,s_q,H,d_r]),
     KV_cache [num_pages,page,d_c], K_pe_cache [num_pages,page,d_r] (bf16),
     block_table [B,max_pages] int32, seqlens [B] int32.  Each sequence gets
     ceil(len / page) pages drawn without replacement from a pool with
@@ -142,8 +143,9 @@ def random_mla_paged(H, seqlens, d_c=512, d_r=64, page=64, spare_pages=3, seed=0
     need = [(n + page - 1) // page for n in lens]
     max_pages = max(1, max(need) if need else 1)
     num_pages = sum(need) + spare_pages
-    Qn = torch.randn(B, H, d_c, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    Qp = torch.randn(B, H, d_r, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    qs = (B, s_q, H) if s_q > 1 else (B, H)
+    Qn = torch.randn(*qs, d_c, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    Qp = torch.randn(*qs, d_r, generator=g, dtype=torch.float32).to(torch.bfloat16)
     KV = torch.randn(num_pages, page, d_c, generator=g, dtype=torch.float32).to(torch.bfloat16)
     Kp = torch.randn(num_pages, page, d_r, generator=g, dtype=torch.float32).to(torch.bfloat16)
     perm = torch.randperm(num_pages, generator=g)
