@@ -282,7 +282,7 @@ def paged_decode_workload(gb, dev, peaks, flush, reps=10):
     B, H = len(lens), 128
     O = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
     LSE = torch.empty(B, H, dtype=torch.float32, device=dev)
-    ws = torch.empty(gb.mla_decode_paged_workspace_bytes(B), dtype=torch.uint8, device=dev)
+    ws = torch.empty(gb.mla_decode_paged_workspace_bytes(B, 1), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(576)
     call = lambda: gb.mla_decode_paged(Qn, Qp, KV, Kp, table, L, scale=scale, O=O, LSE=LSE, workspace=ws)
     for _ in range(3):

@@ -135,11 +135,11 @@ int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_latent, cons
 
 /*
  * mla_decode_paged_workspace_bytes -- size of the scratch buffer
- * mla_decode_paged needs for B sequences on the current device (it depends
- * on the device's SM count, not on the lengths).  Returns 0 for an invalid
- * shape.
+ * mla_decode_paged needs for B sequences of s_q query tokens on the current
+ * device (it depends on the device's SM count, not on the lengths).  Returns
+ * 0 for an invalid shape.
  */
-size_t mla_decode_paged_workspace_bytes(int B, int H, int d_c);
+size_t mla_decode_paged_workspace_bytes(int B, int s_q, int H, int d_c);
 
 /*
  * mla_decode_paged -- MLA decode over a paged KV cache, each sequence with
@@ -148,20 +148,24 @@ size_t mla_decode_paged_workspace_bytes(int B, int H, int d_c);
  * Operation: mla_decode's, with the FlashMLA article's KV loop bound
  * (section 2.2, ceildiv(seqlen_kv, block_N)) taken per sequence: sequence b
  * has keys j < cache_seqlens[b], and key j is row j % 64 of page
- * block_table[b * max_pages_per_seq + j / 64] of the caches.  A sequence of
- * length 0 gets O = 0 and LSE = -inf.
+ * block_table[b * max_pages_per_seq + j / 64] of the caches.  With s_q query
+ * tokens per sequence (several new tokens at once), the tokens are the last
+ * s_q positions of the sequence and attend causally: token t sees keys
+ * j < cache_seqlens[b] - (s_q - 1 - t).  A row without keys gets O = 0 and
+ * LSE = -inf.  Each query token reads the sequence's keys once (the key
+ * tiles are not shared between the tokens of a sequence).
  *
  * Arguments
- *   Q_nope bf16 [B, H, d_c]   Q_pe bf16 [B, H, d_r]
+ *   Q_nope bf16 [B, s_q, H, d_c]   Q_pe bf16 [B, s_q, H, d_r]
  *   KV_cache bf16 [num_pages, 64, d_c]   K_pe_cache bf16 [num_pages, 64, d_r]
  *   block_table int32 [B, max_pages_per_seq] (device; entries past a
  *     sequence's last page are not read)
  *   cache_seqlens int32 [B] (device; 0 <= len <= 64 * max_pages_per_seq)
- *   O bf16 [B, H, d_c] (written)    LSE fp32 [B, H] (written)
- *   page_size = 64, d_c = 512, d_r = 64, H = 128, B >= 1, num_pages >= 1,
- *   max_pages_per_seq >= 1, scale finite and > 0.
+ *   O bf16 [B, s_q, H, d_c] (written)    LSE fp32 [B, s_q, H] (written)
+ *   page_size = 64, d_c = 512, d_r = 64, H = 128, B >= 1, s_q >= 1,
+ *   num_pages >= 1, max_pages_per_seq >= 1, scale finite and > 0.
  *   workspace: device buffer of at least mla_decode_paged_workspace_bytes(B,
- *   H, d_c) bytes, 16-byte aligned, owned by the caller, overwritten; calls
+ *   s_q, H, d_c) bytes, 16-byte aligned, owned by the caller, overwritten; calls
  *   that share a workspace must not overlap in time.
  * Rows of a sequence's last page past its length may hold anything (they
  * are zeroed on chip before the P V product).  The lengths are read on the
@@ -170,8 +174,8 @@ size_t mla_decode_paged_workspace_bytes(int B, int H, int d_c);
  * outside [0, num_pages) reads zeros.
  */
 int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
-                     const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
-                     int num_pages, int max_pages_per_seq, int page_size, int d_c, int d_r, float scale,
+                     const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int s_q,
+                     int H, int num_pages, int max_pages_per_seq, int page_size, int d_c, int d_r, float scale,
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*

@@ -92,7 +92,7 @@ def test_mla_decode_paged_argument_errors(lib):
 
     def paged(B=2, H=128, num_pages=4, max_pages=2, page=64, d_c=512, d_r=64, scale=0.04, Qn=16, table=16,
               lens=16, ws=16):
-        return lib.mla_decode_paged(vp(Qn), vp(16), vp(16), vp(16), vp(table), vp(lens), vp(16), vp(16), B, H,
+        return lib.mla_decode_paged(vp(Qn), vp(16), vp(16), vp(16), vp(table), vp(lens), vp(16), vp(16), B, 1, H,
                                     num_pages, max_pages, page, d_c, d_r, ctypes.c_float(scale), vp(ws), 1 << 20,
                                     None)
     assert paged(B=0) == 1

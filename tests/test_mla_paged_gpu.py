@@ -122,3 +122,14 @@ def test_varied_lengths_full_size_sampled():
     O_ref, L_ref = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, SCALE, rows=rows)
     idx = torch.as_tensor(rows, device=O.device)
     compare(O.reshape(-1, 512)[idx], LSE.reshape(-1)[idx], O_ref, L_ref, what="64 varied sequences")
+
+
+@pytest.mark.parametrize("s_q,lens", [(2, [5, 70, 130, 1, 4097]), (3, [2, 64, 65, 1000]), (4, [3000, 0, 129])],
+                         ids=lambda v: str(v))
+def test_several_query_tokens(s_q, lens):
+    Qn, Qp, KV, Kp, table, L = wl.random_mla_paged(128, lens, seed=70 + s_q, s_q=s_q)
+    O, LSE = run_paged(Qn, Qp, KV, Kp, table, L)
+    assert O.shape == (len(lens), s_q, 128, 512) and LSE.shape == (len(lens), s_q, 128)
+    O_ref, L_ref = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, SCALE)
+    compare(O.reshape(-1, 128, 512), LSE.reshape(-1, 128), O_ref.reshape(-1, 128, 512), L_ref.reshape(-1, 128),
+            what=f"s_q={s_q} lens={lens}")

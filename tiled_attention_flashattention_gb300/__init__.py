@@ -57,9 +57,9 @@ def load_library():
         lib.mla_decode_workspace_bytes.restype = SZ
         lib.mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
         lib.mla_decode.restype = I
-        lib.mla_decode_paged_workspace_bytes.argtypes = [I, I, I]
+        lib.mla_decode_paged_workspace_bytes.argtypes = [I, I, I, I]
         lib.mla_decode_paged_workspace_bytes.restype = SZ
-        lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, SZ, P]
         lib.mla_decode_paged.restype = I
         lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.mla_decode_noalloc.restype = I
@@ -204,26 +204,33 @@ def mla_decode(Q_nope, Q_pe, KV_latent, K_pe, scale: float | None = None, O=None
     return O, LSE
 
 
-def mla_decode_paged_workspace_bytes(B: int, H: int = 128, d_c: int = 512) -> int:
-    return int(load_library().mla_decode_paged_workspace_bytes(B, H, d_c))
+def mla_decode_paged_workspace_bytes(B: int, s_q: int = 1, H: int = 128, d_c: int = 512) -> int:
+    return int(load_library().mla_decode_paged_workspace_bytes(B, s_q, H, d_c))
 
 
 def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seqlens, scale: float | None = None,
                      O=None, LSE=None, workspace=None, stream=None):
     """MLA decode over a paged KV cache with per-sequence lengths.
 
-    Q_nope [B,H,d_c], Q_pe [B,H,d_r], KV_cache [num_pages,64,d_c], K_pe_cache
-    [num_pages,64,d_r] (bf16); block_table [B,max_pages] and cache_seqlens [B]
-    (int32), all CUDA tensors.  Key j of sequence b is row j % 64 of page
-    block_table[b, j // 64].  Returns (O [B,H,d_c] bf16, LSE [B,H] fp32).
+    Q_nope [B,H,d_c] or [B,s_q,H,d_c], Q_pe [B,(s_q,)H,d_r], KV_cache
+    [num_pages,64,d_c], K_pe_cache [num_pages,64,d_r] (bf16); block_table
+    [B,max_pages] and cache_seqlens [B] (int32), all CUDA tensors.  Key j of
+    sequence b is row j % 64 of page block_table[b, j // 64]; with s_q query
+    tokens, token t sees keys j < len - (s_q - 1 - t).  Returns (O, LSE), O
+    bf16 shaped like Q_nope with last dim d_c, LSE fp32 without it.
     """
     lib = load_library()
-    B, H, d_c = Q_nope.shape
+    multi = Q_nope.dim() == 4
+    if multi:
+        B, s_q, H, d_c = Q_nope.shape
+    else:
+        (B, H, d_c), s_q = Q_nope.shape, 1
+    lead = (B, s_q, H) if multi else (B, H)
     d_r = Q_pe.shape[-1]
     num_pages, page, _ = KV_cache.shape
     max_pages = block_table.shape[1]
     _need(Q_nope, "Q_nope", torch.bfloat16, None)
-    _need(Q_pe, "Q_pe", torch.bfloat16, (B, H, d_r))
+    _need(Q_pe, "Q_pe", torch.bfloat16, (*lead, d_r))
     _need(KV_cache, "KV_cache", torch.bfloat16, (num_pages, page, d_c))
     _need(K_pe_cache, "K_pe_cache", torch.bfloat16, (num_pages, page, d_r))
     _need(block_table, "block_table", torch.int32, (B, max_pages))
@@ -231,18 +238,19 @@ def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seql
     if scale is None:
         scale = 1.0 / math.sqrt(d_c + d_r)
     if O is None:
-        O = torch.empty((B, H, d_c), dtype=torch.bfloat16, device=Q_nope.device)
+        O = torch.empty((*lead, d_c), dtype=torch.bfloat16, device=Q_nope.device)
     if LSE is None:
-        LSE = torch.empty((B, H), dtype=torch.float32, device=Q_nope.device)
-    _need(O, "O", torch.bfloat16, (B, H, d_c))
-    _need(LSE, "LSE", torch.float32, (B, H))
-    need = int(lib.mla_decode_paged_workspace_bytes(B, H, d_c))
+        LSE = torch.empty(lead, dtype=torch.float32, device=Q_nope.device)
+    _need(O, "O", torch.bfloat16, (*lead, d_c))
+    _need(LSE, "LSE", torch.float32, lead)
+    need = int(lib.mla_decode_paged_workspace_bytes(B, s_q, H, d_c))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=Q_nope.device)
     _need(workspace, "workspace", torch.uint8, None)
     rc = lib.mla_decode_paged(_ptr(Q_nope), _ptr(Q_pe), _ptr(KV_cache), _ptr(K_pe_cache), _ptr(block_table),
-                              _ptr(cache_seqlens), _ptr(O), _ptr(LSE), B, H, num_pages, max_pages, page, d_c, d_r,
-                              float(scale), _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream_handle(stream)))
+                              _ptr(cache_seqlens), _ptr(O), _ptr(LSE), B, s_q, H, num_pages, max_pages, page, d_c,
+                              d_r, float(scale), _ptr(workspace), workspace.numel(),
+                              ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return O, LSE
 

@@ -239,29 +239,29 @@ extern "C" int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const vo
     return rc;
 }
 
-extern "C" size_t mla_decode_paged_workspace_bytes(int B, int H, int d_c)
+extern "C" size_t mla_decode_paged_workspace_bytes(int B, int s_q, int H, int d_c)
 {
-    if (B < 1 || H < 1 || d_c < 1) return 0;
+    if (B < 1 || s_q < 1 || H < 1 || d_c < 1) return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
-    return mla_paged_workspace_bytes(B, H, d_c, sms);
+    return mla_paged_workspace_bytes(B, s_q, H, d_c, sms);
 }
 
 extern "C" int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
-                                const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
-                                int num_pages, int max_pages_per_seq, int page_size, int d_c, int d_r, float scale,
-                                void *workspace, size_t workspace_bytes, void *stream)
+                                const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int s_q,
+                                int H, int num_pages, int max_pages_per_seq, int page_size, int d_c, int d_r,
+                                float scale, void *workspace, size_t workspace_bytes, void *stream)
 {
     g_err.clear();
-    if (B < 1 || H < 1 || num_pages < 1 || max_pages_per_seq < 1 || d_c < 1 || d_r < 0 || page_size < 1)
-        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_paged: need B, H, num_pages, max_pages_per_seq, d_c, "
+    if (B < 1 || s_q < 1 || H < 1 || num_pages < 1 || max_pages_per_seq < 1 || d_c < 1 || d_r < 0 || page_size < 1)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_paged: need B, s_q, H, num_pages, max_pages_per_seq, d_c, "
                                             "page_size >= 1 and d_r >= 0");
     if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_paged: scale must be finite and > 0");
     if (d_c != 512 || d_r != 64 || H != 128 || page_size != 64)
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_paged: supports d_c = 512, d_r = 64, H = 128, page_size = 64");
-    if (static_cast<long long>(B) * max_pages_per_seq > 0x7fffffffLL ||
+    if (static_cast<long long>(B) * s_q * max_pages_per_seq > 0x7fffffffLL ||
         static_cast<long long>(max_pages_per_seq) * page_size > 0x7fffffffLL)
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_paged: problem too large");
     if (!Q_nope || !Q_pe || !KV_cache || !K_pe_cache || !block_table || !cache_seqlens || !O || !LSE)
@@ -274,12 +274,12 @@ extern "C" int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void
     LaunchEnv env;
     int rc = get_env(env, stream);
     if (rc != GBATTN_OK) return rc;
-    const size_t need = mla_paged_workspace_bytes(B, H, d_c, env.num_sms);
+    const size_t need = mla_paged_workspace_bytes(B, s_q, H, d_c, env.num_sms);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(GBATTN_ERR_WORKSPACE, "mla_decode_paged: workspace missing, smaller than "
                                           "mla_decode_paged_workspace_bytes() or not 16-byte aligned");
     std::string err;
-    rc = launch_mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seqlens, O, LSE, B, H,
+    rc = launch_mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seqlens, O, LSE, B, s_q, H,
                                  num_pages, max_pages_per_seq, d_c, d_r, scale, workspace, workspace_bytes, env,
                                  err);
     if (rc != GBATTN_OK) g_err = err;

@@ -41,10 +41,10 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
                       std::string &err);
 
 // MLA decode over a paged KV cache with per-sequence lengths (mla_decode_paged).
-size_t mla_paged_workspace_bytes(int B, int H, int d_c, int num_sms);
+size_t mla_paged_workspace_bytes(int B, int s_q, int H, int d_c, int num_sms);
 int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
-                            const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
-                            int num_pages, int max_pages, int d_c, int d_r, float scale, void *workspace,
+                            const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int s_q,
+                            int H, int num_pages, int max_pages, int d_c, int d_r, float scale, void *workspace,
                             size_t workspace_bytes, const LaunchEnv &env, std::string &err);
 
 // MLA decode through the library's built-in scratch instead of a workspace

@@ -109,8 +109,10 @@ struct Params {
     // Paged form only (sequences of their own lengths, 64-key pages):
     const int *tile_start;    // [B + 1] first flat tile of each sequence; tile_start[B] = all tiles
     const int *seq_len;       // [B] keys of each sequence (clamped to the block table's capacity)
-    const int *block_table;   // [B][max_pages] page of each 64-key tile
+    const int *block_table;   // [B / q_per_seq][max_pages] page of each 64-key tile
     int max_pages;
+    int q_per_seq;            // query tokens per sequence: entry b is token b % q_per_seq of
+                              // sequence b / q_per_seq (B counts (sequence, token) pairs)
     int max_seg;        // workspace slots per cluster (2: its first and last range)
     float c;            // scale * log2(e)
     int *status;
@@ -274,7 +276,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const long long P0 = S.start(b);
                 const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
                 if (x0 >= x1) continue;       // an empty sequence
-                const int *pages = kPaged ? p.block_table + static_cast<size_t>(b) * p.max_pages : nullptr;
+                const int *pages =
+                    kPaged ? p.block_table + static_cast<size_t>(b / p.q_per_seq) * p.max_pages : nullptr;
                 // paged: the page of the next tile, loaded one tile ahead of its use
                 int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : b;
                 // This sequence's query part: two ring slots, each [128 heads x 64 dims]
@@ -304,7 +307,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const long long nn = min(S.start(nb + 1), t_end) - x1;
                         for (int j = 0; j < min(nn, 3LL); ++j) {
                             const int r = kPaged ? 0 : j * kBN;
-                            const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(nb) * p.max_pages + j) : nb;
+                            const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(nb / p.q_per_seq) * p.max_pages + j)
+                                                 : nb;
                             for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, r, o);
                             if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, r, o);
                         }
@@ -807,11 +811,13 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     if (threadIdx.x % 16 == 0) p.LSE[static_cast<size_t>(b) * kH + h] = lse;
 }
 
-// Paged form: per-sequence key counts (clamped to the block table's capacity;
-// a length outside [0, capacity] sets the status word) and the exclusive
-// prefix sum of their 64-key tile counts, tile_start[0..B].  One block.
+// Paged form: the key count of every (sequence, query token) entry b (token
+// t = b % s_q of sequence b / s_q sees keys < len - (s_q - 1 - t); lengths
+// outside [0, capacity] are clamped and set the status word) and the
+// exclusive prefix sum of their 64-key tile counts, tile_start[0..B].  One
+// block.
 __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlens, int *seq_len, int *tile_start,
-                                                        int B, int capacity, int *status)
+                                                        int B, int s_q, int capacity, int *status)
 {
     __shared__ int warp_sum[32];
     __shared__ int carry;
@@ -823,11 +829,12 @@ __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlen
         const int b = base + threadIdx.x;
         int n = 0;
         if (b < B) {
-            int len = cache_seqlens[b];
+            int len = cache_seqlens[b / s_q];
             if (len < 0 || len > capacity) {
-                atomicCAS(status, 0, kStatusBadLength);
+                if (b % s_q == 0) atomicCAS(status, 0, kStatusBadLength);
                 len = min(max(len, 0), capacity);
             }
+            len = max(len - (s_q - 1 - b % s_q), 0);
             seq_len[b] = len;
             n = (len + kBN - 1) / kBN;
         }
@@ -1010,6 +1017,7 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     p.seq_len = nullptr;
     p.block_table = nullptr;
     p.max_pages = 0;
+    p.q_per_seq = 1;
     cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
@@ -1047,18 +1055,19 @@ static size_t paged_bytes(int B, int clusters, size_t &off_tiles)
     return off_tiles + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
 }
 
-size_t mla_paged_workspace_bytes(int B, int H, int d_c, int num_sms)
+size_t mla_paged_workspace_bytes(int B, int s_q, int H, int d_c, int num_sms)
 {
-    if (B < 1 || H != kH || d_c != kDc) return 0;
+    if (B < 1 || s_q < 1 || H != kH || d_c != kDc) return 0;
     size_t off = 0;
-    return paged_bytes(B, resident_clusters(num_sms), off);
+    return paged_bytes(B * s_q, resident_clusters(num_sms), off);
 }
 
 int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
-                            const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B, int H,
-                            int num_pages, int max_pages, int d_c, int d_r, float scale, void *workspace,
-                            size_t workspace_bytes, const LaunchEnv &env, std::string &err)
+                            const int *block_table, const int *cache_seqlens, void *O, float *LSE, int B_seq,
+                            int s_q, int H, int num_pages, int max_pages, int d_c, int d_r, float scale,
+                            void *workspace, size_t workspace_bytes, const LaunchEnv &env, std::string &err)
 {
+    const int B = B_seq * s_q;           // (sequence, query token) entries
     const int C = resident_clusters(env.num_sms);
     size_t off_tiles = 0;
     if (workspace_bytes < paged_bytes(B, C, off_tiles)) {
@@ -1091,7 +1100,9 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
     p.seq_len = seq_len;
     p.block_table = block_table;
     p.max_pages = max_pages;
-    mla_tiles_kernel<<<1, 1024, 0, env.stream>>>(cache_seqlens, seq_len, tile_start, B, max_pages * kBN, env.status);
+    p.q_per_seq = s_q;
+    mla_tiles_kernel<<<1, 1024, 0, env.stream>>>(cache_seqlens, seq_len, tile_start, B, s_q, max_pages * kBN,
+                                                 env.status);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mla_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
