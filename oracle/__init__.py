@@ -49,6 +49,8 @@ def _load():
             lib.oracle_attn_fwd.restype = I
             lib.oracle_attn_fwd_masked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I, P, I64, I]
             lib.oracle_attn_fwd_masked.restype = I
+            lib.oracle_ssd_scan.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I]
+            lib.oracle_ssd_scan.restype = I
             lib.oracle_mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, D, P, I64, I]
             lib.oracle_mla_decode.restype = I
             lib.oracle_mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I64, I]
@@ -189,3 +191,23 @@ def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, seqlens, s
         O = O.reshape(B, s_q, H, d_c) if multi else O.reshape(B, H, d_c)
         LSE = LSE.reshape(B, s_q, H) if multi else LSE.reshape(B, H)
     return O, LSE
+
+
+def ssd_scan(x, dt, A, B, C, D=None, threads: int | None = None):
+    """Reference Mamba-2 SSD scan (plain recurrence in fp64): x [Bsz,L,H,P] bf16,
+    dt [Bsz,L,H] fp32, A [H] fp32, B, C [Bsz,L,G,N] bf16, D [H] fp32 or None.
+    Returns (y [Bsz,L,H,P], final state [Bsz,H,P,N]) as float64 numpy arrays."""
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    xb, Bb, Cb = _bf16_bits(x), _bf16_bits(B), _bf16_bits(C)
+    f32 = lambda t: np.ascontiguousarray(t.detach().cpu().to(torch.float32).numpy())
+    dtn, An = f32(dt), f32(A)
+    Dn = f32(D) if D is not None else None
+    y = np.zeros((Bsz, L, H, P), dtype=np.float64)
+    S = np.zeros((Bsz, H, P, N), dtype=np.float64)
+    rc = _load().oracle_ssd_scan(_ptr(xb), _ptr(dtn), _ptr(An), _ptr(Bb), _ptr(Cb),
+                                 _ptr(Dn) if Dn is not None else None, _ptr(y), _ptr(S),
+                                 Bsz, L, H, P, G, N, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_ssd_scan rejected its arguments")
+    return y, S

@@ -396,3 +396,78 @@ int oracle_mla_decode_paged(const uint16_t *Q_nope, const uint16_t *Q_pe, const 
     free(jobs);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Mamba-2 SSD scan (the chunk-state / chunk-scan linear-attention functions */
+/* named in "TileLang: 面向AI系统的可组合分块编程模型" (results, linear        */
+/* attention on H100), with the selective-scan recurrence sketched in        */
+/* "从FlashAttention到通用内核" section 4), written as the plain recurrence:  */
+/* per batch b and head h (group g = h / (H / G)), with state S [P][N]:      */
+/*   S_t = exp(dt_t * A_h) * S_{t-1} + dt_t * x_t (outer) B_t                */
+/*   y_t = S_t . C_t  (+ D_h * x_t)                                          */
+/* x [B][L][H][P] bf16, dt [B][L][H] fp32, A [H] fp32, B_, C_ [B][L][G][N]   */
+/* bf16, D [H] fp32 or NULL; y [B][L][H][P] and the final state             */
+/* [B][H][P][N] (may be NULL) in fp64.                                       */
+
+static double f32_to_f64(float f) { return (double)f; }
+
+typedef struct {
+    const uint16_t *x, *Bm, *Cm;
+    const float *dt, *A, *D;
+    double *y, *S_out;
+    int Bsz, L, H, P, G, N;
+    int n_threads, tid;
+} ssd_job;
+
+static void *ssd_worker(void *arg)
+{
+    const ssd_job *J = (const ssd_job *)arg;
+    const int P = J->P, N = J->N, H = J->H, G = J->G, L = J->L;
+    double *S = (double *)malloc(sizeof(double) * (size_t)P * N);
+    if (!S) return (void *)1;
+    for (long bh = J->tid; bh < (long)J->Bsz * H; bh += J->n_threads) {
+        const long b = bh / H, h = bh % H, g = h / (H / G);
+        for (long i = 0; i < (long)P * N; i++) S[i] = 0.0;
+        for (long t = 0; t < L; t++) {
+            const double dt = f32_to_f64(J->dt[(b * L + t) * H + h]);
+            const double decay = exp(dt * f32_to_f64(J->A[h]));
+            const uint16_t *xt = J->x + ((b * L + t) * H + h) * P;
+            const uint16_t *Bt = J->Bm + ((b * L + t) * G + g) * N;
+            const uint16_t *Ct = J->Cm + ((b * L + t) * G + g) * N;
+            double *yt = J->y + ((b * L + t) * H + h) * P;
+            for (int p = 0; p < P; p++) {
+                const double xp = bf16_to_f64(xt[p]);
+                double acc = 0.0;
+                for (int n = 0; n < N; n++) {
+                    double *s = S + (long)p * N + n;
+                    *s = decay * *s + dt * xp * bf16_to_f64(Bt[n]);
+                    acc += *s * bf16_to_f64(Ct[n]);
+                }
+                yt[p] = acc + (J->D ? f32_to_f64(J->D[h]) * xp : 0.0);
+            }
+        }
+        if (J->S_out) memcpy(J->S_out + bh * (long)P * N, S, sizeof(double) * (size_t)P * N);
+    }
+    free(S);
+    return NULL;
+}
+
+int oracle_ssd_scan(const uint16_t *x, const float *dt, const float *A, const uint16_t *Bm, const uint16_t *Cm,
+                    const float *D, double *y, double *S_out, int Bsz, int L, int H, int P, int G, int N,
+                    int n_threads)
+{
+    if (Bsz < 0 || L < 0 || H <= 0 || P <= 0 || G <= 0 || N <= 0 || H % G) return -1;
+    const long total = (long)Bsz * H;
+    if (total == 0) return 0;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > total) n_threads = (int)total;
+    ssd_job *jobs = (ssd_job *)malloc(sizeof(ssd_job) * n_threads);
+    if (!jobs) return -1;
+    for (int t = 0; t < n_threads; t++) {
+        ssd_job j = {x, Bm, Cm, dt, A, D, y, S_out, Bsz, L, H, P, G, N, n_threads, t};
+        jobs[t] = j;
+    }
+    int rc = run_threads(ssd_worker, jobs, sizeof(ssd_job), n_threads);
+    free(jobs);
+    return rc;
+}

@@ -163,3 +163,17 @@ def random_block_mask(B, H, N_q, N_kv, density, seed, block=128):
     g = _gen(seed)
     shape = (B, H, -(-N_q // block), -(-N_kv // block))
     return (torch.rand(*shape, generator=g) < density).to(torch.uint8)
+
+
+def random_ssd(Bsz, L, H, P, G, N, seed, with_D=True):
+    """Mamba-2 SSD scan inputs (torch CPU generator): x [Bsz,L,H,P] bf16 ~ N(0,1);
+    dt [Bsz,L,H] fp32 log-uniform in [0.001, 0.1]; A [H] fp32 = -exp(U[0, ln 16]);
+    B, C [Bsz,L,G,N] bf16 ~ N(0,1); D [H] fp32 = 1 (or None)."""
+    g = _gen(seed)
+    x = torch.randn(Bsz, L, H, P, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dt = torch.exp(torch.rand(Bsz, L, H, generator=g) * (math.log(0.1) - math.log(0.001)) + math.log(0.001))
+    A = -torch.exp(torch.rand(H, generator=g) * math.log(16.0))
+    B = torch.randn(Bsz, L, G, N, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    C = torch.randn(Bsz, L, G, N, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    D = torch.ones(H, dtype=torch.float32) if with_D else None
+    return x, dt.to(torch.float32), A.to(torch.float32), B, C, D
