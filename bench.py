@@ -355,6 +355,60 @@ def sparse_prefill_workload(gb, dev, peaks, flush, reps=10):
             "active_blocks": int(mask_h.sum()), "algorithmic_flops": flops}
 
 
+# FP32 FFMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz.
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def ssd_flops(c) -> float:
+    """FLOPs of the chunked SSD scan (64-step chunks): per (chunk, head) the
+    chunk state 2QPN, the entering-state product C S 2QPN, and the causal
+    intra-chunk products C B^T and W x over the Q(Q+1)/2 pairs s <= t (2N and
+    2P FLOPs per pair); the ragged last chunk counts its own length."""
+    Q, total = 64, 0.0
+    for c0 in range(0, c.L, Q):
+        q = min(Q, c.L - c0)
+        total += 4.0 * q * c.P * c.N + q * (q + 1) * (c.N + c.P)
+    return total * c.Bsz * c.H
+
+
+def ssd_bytes(c) -> float:
+    """Algorithmic bytes: x (bf16) read and y (fp32) written once, dt read once,
+    B and C (bf16) read once per group."""
+    return float(c.Bsz * c.L * (c.H * (2 * c.P + 4 * c.P + 4) + c.G * 2 * 2 * c.N))
+
+
+def ssd_workload(gb, dev, flush, reps=10):
+    """Kernel-only throughput of ssd_scan (three kernels) on the Mamba-2-sized
+    workload, inputs resident, L2 flushed before each timed call, CUDA events
+    around the call.  The path runs on the FP32 CUDA cores, so the roofline is
+    the FFMA peak."""
+    c = wl.SSD_WORKLOAD
+    x, dt, A, B, C, D = (t.to(dev) for t in wl.ssd_inputs(c))
+    y = torch.empty(c.Bsz, c.L, c.H, c.P, dtype=torch.float32, device=dev)
+    S = torch.empty(c.Bsz, c.H, c.P, c.N, dtype=torch.float32, device=dev)
+    ws = torch.empty(gb.ssd_scan_workspace_bytes(c.Bsz, c.L, c.H, c.P, c.N), dtype=torch.uint8, device=dev)
+    call = lambda: gb.ssd_scan(x, dt, A, B, C, D, y=y, final_state=S, workspace=ws)
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream(dev)
+    total = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    gb.check()
+    t = total / reps
+    tf = ssd_flops(c) / t / 1e12
+    del x, y, S, ws
+    return {"workload": c.name, "tflops": tf, "bound": "alu", "peak_tflops": FP32_ALU_TFLOPS,
+            "frac_alu_peak": tf / FP32_ALU_TFLOPS, "ms": t * 1e3, "gbs": ssd_bytes(c) / t / 1e9,
+            "algorithmic_flops": ssd_flops(c), "algorithmic_bytes": ssd_bytes(c), "launches_per_call": 3}
+
+
 def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
     """Kernel-only TFLOP/s of the other prefill workloads (inputs resident,
     L2 flushed before each timed launch, CUDA events around the launch)."""
@@ -536,6 +590,7 @@ def run_ours(args, rank, world, local):
         line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
         line["decode_paged"] = paged_decode_workload(gb, dev, peaks, flush)
         line["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks, flush)
+        line["ssd_scan"] = ssd_workload(gb, dev, flush)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)

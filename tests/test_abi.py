@@ -103,3 +103,23 @@ def test_mla_decode_paged_argument_errors(lib):
     assert paged(table=0) == 1                     # null block table
     assert paged(lens=18) == 3                     # misaligned lengths
     assert paged(Qn=40) == 3
+
+
+def test_ssd_scan_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def ssd(Bsz=2, L=100, H=4, P=64, G=2, N=128, x=16, dt=16, D=16, y=16, fs=16):
+        return lib.ssd_scan(vp(x), vp(dt), vp(16), vp(16), vp(16), vp(D), vp(y), vp(fs), Bsz, L, H, P, G, N,
+                            vp(16), 1 << 30, None)
+    assert ssd(Bsz=0) == 1
+    assert ssd(L=0) == 1
+    assert ssd(G=3) == 1                           # H % G != 0
+    assert ssd(P=128) == 2                         # head dim other than 64
+    assert ssd(N=64) == 2                          # state dim other than 128
+    assert ssd(x=0) == 1
+    assert ssd(x=40) == 3                          # misaligned x
+    assert ssd(fs=20) == 3                         # misaligned final state
+    assert ssd(dt=18) == 3                         # dt not 4-byte aligned
+    assert ssd(D=0, fs=0) not in (1, 3)            # D and the final state may be omitted
+    assert lib.ssd_scan_workspace_bytes(2, 100, 4, 64, 128) == 2 * 2 * 4 * (64 * 128 + 1) * 4
+    assert lib.ssd_scan_workspace_bytes(2, 100, 4, 32, 128) == 0

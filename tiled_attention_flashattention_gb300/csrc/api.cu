@@ -286,6 +286,43 @@ extern "C" int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void
     return rc;
 }
 
+extern "C" size_t ssd_scan_workspace_bytes(int Bsz, int L, int H, int P, int N)
+{
+    if (Bsz < 1 || L < 1 || H < 1 || P != 64 || N != 128) return 0;
+    return ssd_workspace_bytes(Bsz, L, H);
+}
+
+extern "C" int ssd_scan(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
+                        float *y, float *final_state, int Bsz, int L, int H, int P, int G, int N, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    g_err.clear();
+    if (Bsz < 1 || L < 1 || H < 1 || G < 1 || P < 1 || N < 1)
+        return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: need Bsz, L, H, G, P, N >= 1");
+    if (H % G != 0) return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: H must be a multiple of G");
+    if (P != 64 || N != 128) return fail(GBATTN_ERR_UNSUPPORTED, "ssd_scan: supports P = 64, N = 128");
+    if (static_cast<long long>(Bsz) * L * H > (1LL << 34))
+        return fail(GBATTN_ERR_UNSUPPORTED, "ssd_scan: problem too large");
+    if (!x || !dt || !A || !B || !C || !y)
+        return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: null tensor pointer");
+    auto al4 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) ||
+        (final_state && !aligned16(final_state)) || !al4(dt) || !al4(A) || (D && !al4(D)))
+        return fail(GBATTN_ERR_ALIGNMENT, "ssd_scan: x, B, C, y, final_state must be 16-byte aligned "
+                                          "(dt, A, D 4-byte)");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    if (!workspace || workspace_bytes < ssd_workspace_bytes(Bsz, L, H) || !aligned16(workspace))
+        return fail(GBATTN_ERR_WORKSPACE, "ssd_scan: workspace missing, smaller than ssd_scan_workspace_bytes() "
+                                          "or not 16-byte aligned");
+    std::string err;
+    rc = launch_ssd_scan(x, dt, A, B, C, D, y, final_state, Bsz, L, H, P, G, N, workspace, workspace_bytes, env,
+                         err);
+    if (rc != GBATTN_OK) g_err = err;
+    return rc;
+}
+
 extern "C" int gbattn_check(void *stream)
 {
     g_err.clear();

@@ -53,6 +53,12 @@ int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *
                               void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
                               const LaunchEnv &env, std::string &err);
 
+// Mamba-2 SSD scan (ssd_scan).
+size_t ssd_workspace_bytes(int Bsz, int L, int H);
+int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *Bm, const void *Cm, const float *D,
+                    float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, void *workspace,
+                    size_t workspace_bytes, const LaunchEnv &env, std::string &err);
+
 // Tensor-core layout self test (gbattn_selftest_umma).
 int launch_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
                          float *O, const LaunchEnv &env, std::string &err);

@@ -80,6 +80,29 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class SsdCase:
+    """Mamba-2 SSD scan shape: batch, sequence length, heads, head dim P,
+    B/C groups G, state dim N."""
+    name: str
+    Bsz: int
+    L: int
+    H: int
+    P: int = 64
+    G: int = 1
+    N: int = 128
+    seed: int = SEED_BASE
+
+
+# A Mamba-2-sized layer (inner width 5120 = 80 heads of 64, state 128, one
+# B/C group) over 8 sequences of 4096 steps.
+SSD_WORKLOAD = SsdCase("ssd_b8_l4096_h80_p64_g1_n128", 8, 4096, 80, seed=SEED_BASE + 7)
+
+
+def ssd_inputs(case: SsdCase):
+    return random_ssd(case.Bsz, case.L, case.H, case.P, case.G, case.N, seed=case.seed)
+
+
 def _gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
