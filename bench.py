@@ -355,19 +355,16 @@ def sparse_prefill_workload(gb, dev, peaks, flush, reps=10):
             "active_blocks": int(mask_h.sum()), "algorithmic_flops": flops}
 
 
-# FP32 FFMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz.
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-
-
 def ssd_flops(c) -> float:
-    """FLOPs of the chunked SSD scan (64-step chunks): per (chunk, head) the
-    chunk state 2QPN, the entering-state product C S 2QPN, and the causal
-    intra-chunk products C B^T and W x over the Q(Q+1)/2 pairs s <= t (2N and
-    2P FLOPs per pair); the ragged last chunk counts its own length."""
-    Q, total = 64, 0.0
+    """FLOPs of the chunked SSD scan (128-step chunks): per (chunk, head) the
+    causal intra-chunk products C B^T and W x over the Q(Q+1)/2 pairs s <= t
+    (2N and 2P FLOPs per pair), the entering-state product C S^T (2QPN) and the
+    chunk's state contribution (2QPN); the ragged last chunk counts its own
+    length."""
+    Q, total = 128, 0.0
     for c0 in range(0, c.L, Q):
         q = min(Q, c.L - c0)
-        total += 4.0 * q * c.P * c.N + q * (q + 1) * (c.N + c.P)
+        total += q * (q + 1) * (c.N + c.P) + 4.0 * q * c.P * c.N
     return total * c.Bsz * c.H
 
 
@@ -377,17 +374,17 @@ def ssd_bytes(c) -> float:
     return float(c.Bsz * c.L * (c.H * (2 * c.P + 4 * c.P + 4) + c.G * 2 * 2 * c.N))
 
 
-def ssd_workload(gb, dev, flush, reps=10):
-    """Kernel-only throughput of ssd_scan (three kernels) on the Mamba-2-sized
-    workload, inputs resident, L2 flushed before each timed call, CUDA events
-    around the call.  The path runs on the FP32 CUDA cores, so the roofline is
-    the FFMA peak."""
+def ssd_workload(gb, dev, peaks, flush, reps=10):
+    """Kernel-only throughput of ssd_scan on the Mamba-2-sized workload, inputs
+    resident, L2 flushed before each timed call, CUDA events around the call.
+    At this size the HBM time floor (algorithmic bytes / copy bandwidth) is
+    about twice the tensor floor (algorithmic FLOPs / bf16 peak), so the
+    roofline is HBM."""
     c = wl.SSD_WORKLOAD
     x, dt, A, B, C, D = (t.to(dev) for t in wl.ssd_inputs(c))
     y = torch.empty(c.Bsz, c.L, c.H, c.P, dtype=torch.float32, device=dev)
     S = torch.empty(c.Bsz, c.H, c.P, c.N, dtype=torch.float32, device=dev)
-    ws = torch.empty(gb.ssd_scan_workspace_bytes(c.Bsz, c.L, c.H, c.P, c.N), dtype=torch.uint8, device=dev)
-    call = lambda: gb.ssd_scan(x, dt, A, B, C, D, y=y, final_state=S, workspace=ws)
+    call = lambda: gb.ssd_scan(x, dt, A, B, C, D, y=y, final_state=S)
     for _ in range(3):
         call()
     stream = torch.cuda.current_stream(dev)
@@ -402,11 +399,13 @@ def ssd_workload(gb, dev, flush, reps=10):
         total += e0.elapsed_time(e1) / 1e3
     gb.check()
     t = total / reps
+    by = ssd_bytes(c) + c.Bsz * c.H * c.P * c.N * 4
+    gbs = by / t / 1e9
     tf = ssd_flops(c) / t / 1e12
-    del x, y, S, ws
-    return {"workload": c.name, "tflops": tf, "bound": "alu", "peak_tflops": FP32_ALU_TFLOPS,
-            "frac_alu_peak": tf / FP32_ALU_TFLOPS, "ms": t * 1e3, "gbs": ssd_bytes(c) / t / 1e9,
-            "algorithmic_flops": ssd_flops(c), "algorithmic_bytes": ssd_bytes(c), "launches_per_call": 3}
+    del x, y, S
+    return {"workload": c.name, "bound": "hbm", "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"], "ms": t * 1e3,
+            "algorithmic_bytes": by, "algorithmic_flops": ssd_flops(c), "launches_per_call": 1}
 
 
 def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
@@ -590,7 +589,7 @@ def run_ours(args, rank, world, local):
         line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
         line["decode_paged"] = paged_decode_workload(gb, dev, peaks, flush)
         line["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks, flush)
-        line["ssd_scan"] = ssd_workload(gb, dev, flush)
+        line["ssd_scan"] = ssd_workload(gb, dev, peaks, flush)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)
@@ -612,6 +611,13 @@ def run_profile_case(args, local):
         LSE = torch.empty(pc.B, pc.H, pc.N_q, dtype=torch.float32, device=dev)
         for _ in range(args.warmup + args.steps):
             gb.attn_fwd(Q, K, V, causal=pc.causal, window=pc.window, scale=pc.softmax_scale(), O=O, LSE=LSE)
+    elif args.profile == "ssd":
+        c = wl.SsdCase(**{**wl.SSD_WORKLOAD.__dict__, "Bsz": args.ssd_batch or wl.SSD_WORKLOAD.Bsz})
+        x, dt, A, B, C, D = (t.to(dev) for t in wl.ssd_inputs(c))
+        y = torch.empty(c.Bsz, c.L, c.H, c.P, dtype=torch.float32, device=dev)
+        S = torch.empty(c.Bsz, c.H, c.P, c.N, dtype=torch.float32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gb.ssd_scan(x, dt, A, B, C, D, y=y, final_state=S)
     else:
         dc = wl.WORKLOADS[args.decode_workload]
         Qn, Qp, KV, Kp = (x.to(dev) for x in wl.mla_inputs(dc))
@@ -638,8 +644,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other prefill workloads")
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "ssd"], default=None,
                     help="only launch the selected kernel warmup+steps times (for ncu captures)")
+    ap.add_argument("--ssd-batch", type=int, default=0,
+                    help="with --profile ssd: batch entries of the SSD workload (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

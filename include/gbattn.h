@@ -209,12 +209,6 @@ int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_late
                        void *stream);
 
 /*
- * ssd_scan_workspace_bytes -- size of the scratch buffer ssd_scan needs
- * (the per-chunk states, fp32).  Returns 0 for an invalid shape.
- */
-size_t ssd_scan_workspace_bytes(int Bsz, int L, int H, int P, int N);
-
-/*
  * ssd_scan -- Mamba-2 SSD scan, the chunk-state / chunk-scan linear-attention
  * functions benchmarked in "TileLang: 面向AI系统的可组合分块编程模型" (results,
  * linear attention on H100), with the selective-scan recurrence sketched in
@@ -222,22 +216,24 @@ size_t ssd_scan_workspace_bytes(int Bsz, int L, int H, int P, int N);
  * g = h / (H / G)), state S [P][N] starting at zero:
  *   S_t = exp(dt_t A_h) S_{t-1} + dt_t x_t (outer) B_t
  *   y_t = S_t C_t + D_h x_t
- * computed in chunks of 64 steps (the state is carried between chunks).
+ * computed in chunks of 128 steps on the tensor cores (the state is carried
+ * between chunks on chip, fp32).  The chunk-internal weights
+ * exp(cum_t - cum_s) dt_s (C_t . B_s), the decayed B rows and the carried
+ * state enter the tensor-core products rounded to bf16; sums are fp32.
  *
  * Arguments
  *   x bf16 [Bsz, L, H, P]   dt fp32 [Bsz, L, H]   A fp32 [H]
  *   B, C bf16 [Bsz, L, G, N]   D fp32 [H] or NULL (no skip term)
  *   y fp32 [Bsz, L, H, P] (written)
  *   final_state fp32 [Bsz, H, P, N] (written) or NULL
- *   P = 64, N = 128, H % G == 0, Bsz, L >= 1.
- *   workspace: device buffer of at least ssd_scan_workspace_bytes(Bsz, L, H,
- *   P, N) bytes, 16-byte aligned, owned by the caller, overwritten.
- * Errors: GBATTN_ERR_INVALID_ARG, _UNSUPPORTED (other P, N), _ALIGNMENT,
- * _WORKSPACE, _LAUNCH; asynchronous on `stream`.
+ *   P = 64, N = 128, H % G == 0, 1 <= Bsz <= 65535, L >= 1.
+ *   All device pointers, caller-owned; no workspace.
+ * Errors: GBATTN_ERR_INVALID_ARG, _UNSUPPORTED (other P, N), _ALIGNMENT
+ * (x, B, C, y, final_state 16-byte; dt, A, D 4-byte), _LAUNCH;
+ * asynchronous on `stream`.
  */
 int ssd_scan(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
-             float *y, float *final_state, int Bsz, int L, int H, int P, int G, int N, void *workspace,
-             size_t workspace_bytes, void *stream);
+             float *y, float *final_state, int Bsz, int L, int H, int P, int G, int N, void *stream);
 
 /*
  * gbattn_check -- synchronise `stream`, then read and clear the device status

@@ -17,7 +17,7 @@ import threading
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_sparse", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_paged",
-           "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan", "ssd_scan_workspace_bytes",
+           "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan",
            "check", "selftest_umma",
            "set_wait_timeout_ns", "set_fault_injection", "GbattnError", "library_path", "load_library"]
 
@@ -63,9 +63,7 @@ def load_library():
         lib.mla_decode_paged_workspace_bytes.restype = SZ
         lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, SZ, P]
         lib.mla_decode_paged.restype = I
-        lib.ssd_scan_workspace_bytes.argtypes = [I, I, I, I, I]
-        lib.ssd_scan_workspace_bytes.restype = SZ
-        lib.ssd_scan.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, SZ, P]
+        lib.ssd_scan.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P]
         lib.ssd_scan.restype = I
         lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.mla_decode_noalloc.restype = I
@@ -261,12 +259,7 @@ def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seql
     return O, LSE
 
 
-def ssd_scan_workspace_bytes(Bsz: int, L: int, H: int, P: int = 64, N: int = 128) -> int:
-    return int(load_library().ssd_scan_workspace_bytes(Bsz, L, H, P, N))
-
-
-def ssd_scan(x, dt, A, B, C, D=None, y=None, final_state=None, want_final_state: bool = False, workspace=None,
-             stream=None):
+def ssd_scan(x, dt, A, B, C, D=None, y=None, final_state=None, want_final_state: bool = False, stream=None):
     """Mamba-2 SSD scan.  x [Bsz,L,H,P] bf16, dt [Bsz,L,H] fp32, A [H] fp32, B, C
     [Bsz,L,G,N] bf16, D [H] fp32 or None (CUDA tensors).  Returns y [Bsz,L,H,P]
     fp32, and the final state [Bsz,H,P,N] fp32 when asked for."""
@@ -287,13 +280,9 @@ def ssd_scan(x, dt, A, B, C, D=None, y=None, final_state=None, want_final_state:
         final_state = torch.empty((Bsz, H, P, N), dtype=torch.float32, device=x.device)
     if final_state is not None:
         _need(final_state, "final_state", torch.float32, (Bsz, H, P, N))
-    need = ssd_scan_workspace_bytes(Bsz, L, H, P, N)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    _need(workspace, "workspace", torch.uint8, None)
     rc = lib.ssd_scan(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D) if D is not None else None, _ptr(y),
-                      _ptr(final_state) if final_state is not None else None, Bsz, L, H, P, G, N, _ptr(workspace),
-                      workspace.numel(), ctypes.c_void_p(_stream_handle(stream)))
+                      _ptr(final_state) if final_state is not None else None, Bsz, L, H, P, G, N,
+                      ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return (y, final_state) if final_state is not None else y
 

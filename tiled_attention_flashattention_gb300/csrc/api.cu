@@ -78,23 +78,31 @@ bool valid_scale(float s)
 
 }  // namespace
 
-bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
-                      uint64_t outer, uint32_t box_rows, std::string &err)
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn tensor_map_encoder()
 {
-    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
     static EncodeFn encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             encode = reinterpret_cast<EncodeFn>(fn);
     });
+    return encode;
+}
+}  // namespace
+
+bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
+                      uint64_t outer, uint32_t box_rows, std::string &err)
+{
+    EncodeFn encode = tensor_map_encoder();
     if (!encode) {
         err = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
@@ -112,6 +120,33 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
         snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu,%llu,%llu] box rows %u",
                  static_cast<int>(r), static_cast<unsigned long long>(outer),
                  static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols), box_rows);
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
+bool make_tma_bf16_4d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[4],
+                      const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
+{
+    EncodeFn encode = tensor_map_encoder();
+    if (!encode) {
+        err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+    const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = encode(&desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), d, st, bx, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[200];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for dims [%llu,%llu,%llu,%llu]",
+                 static_cast<int>(r), static_cast<unsigned long long>(dims[3]),
+                 static_cast<unsigned long long>(dims[2]), static_cast<unsigned long long>(dims[1]),
+                 static_cast<unsigned long long>(dims[0]));
         err = buf;
         return false;
     }
@@ -286,23 +321,15 @@ extern "C" int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void
     return rc;
 }
 
-extern "C" size_t ssd_scan_workspace_bytes(int Bsz, int L, int H, int P, int N)
-{
-    if (Bsz < 1 || L < 1 || H < 1 || P != 64 || N != 128) return 0;
-    return ssd_workspace_bytes(Bsz, L, H);
-}
-
 extern "C" int ssd_scan(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
-                        float *y, float *final_state, int Bsz, int L, int H, int P, int G, int N, void *workspace,
-                        size_t workspace_bytes, void *stream)
+                        float *y, float *final_state, int Bsz, int L, int H, int P, int G, int N, void *stream)
 {
     g_err.clear();
     if (Bsz < 1 || L < 1 || H < 1 || G < 1 || P < 1 || N < 1)
         return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: need Bsz, L, H, G, P, N >= 1");
     if (H % G != 0) return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: H must be a multiple of G");
     if (P != 64 || N != 128) return fail(GBATTN_ERR_UNSUPPORTED, "ssd_scan: supports P = 64, N = 128");
-    if (static_cast<long long>(Bsz) * L * H > (1LL << 34))
-        return fail(GBATTN_ERR_UNSUPPORTED, "ssd_scan: problem too large");
+    if (Bsz > 65535) return fail(GBATTN_ERR_UNSUPPORTED, "ssd_scan: Bsz > 65535");
     if (!x || !dt || !A || !B || !C || !y)
         return fail(GBATTN_ERR_INVALID_ARG, "ssd_scan: null tensor pointer");
     auto al4 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
@@ -313,12 +340,8 @@ extern "C" int ssd_scan(const void *x, const float *dt, const float *A, const vo
     LaunchEnv env;
     int rc = get_env(env, stream);
     if (rc != GBATTN_OK) return rc;
-    if (!workspace || workspace_bytes < ssd_workspace_bytes(Bsz, L, H) || !aligned16(workspace))
-        return fail(GBATTN_ERR_WORKSPACE, "ssd_scan: workspace missing, smaller than ssd_scan_workspace_bytes() "
-                                          "or not 16-byte aligned");
     std::string err;
-    rc = launch_ssd_scan(x, dt, A, B, C, D, y, final_state, Bsz, L, H, P, G, N, workspace, workspace_bytes, env,
-                         err);
+    rc = launch_ssd_scan(x, dt, A, B, C, D, y, final_state, Bsz, L, H, P, G, N, env, err);
     if (rc != GBATTN_OK) g_err = err;
     return rc;
 }

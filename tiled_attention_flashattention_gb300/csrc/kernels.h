@@ -54,10 +54,9 @@ int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *
                               const LaunchEnv &env, std::string &err);
 
 // Mamba-2 SSD scan (ssd_scan).
-size_t ssd_workspace_bytes(int Bsz, int L, int H);
 int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *Bm, const void *Cm, const float *D,
-                    float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, void *workspace,
-                    size_t workspace_bytes, const LaunchEnv &env, std::string &err);
+                    float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, const LaunchEnv &env,
+                    std::string &err);
 
 // Tensor-core layout self test (gbattn_selftest_umma).
 int launch_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
@@ -69,5 +68,9 @@ int launch_selftest_umma(const void *A, const void *B, const void *P, const void
 // Returns false and fills err on failure.
 bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t outer, uint32_t box_rows, std::string &err);
+// 4-D bf16 tensor map, 128-byte swizzle; dims innermost first, strides in bytes
+// of dims 1..3, box in elements (box[0] * 2 bytes = 128).
+bool make_tma_bf16_4d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[4],
+                      const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err);
 
 }  // namespace gbattn

@@ -10,10 +10,29 @@
 //           + exp(cum_t) S_in C_t + D x_t,
 // and the state the chunk passes on is
 //     S_out = exp(cum_end) S_in + sum_s exp(cum_end - cum_s) dt_s x_s B_s^T.
-// Three kernels: the per-chunk state contributions (chunk_state), the
-// sequential state passing over chunks (state_pass, in place: each chunk's
-// slot ends up holding the state entering it) and the chunk outputs
-// (chunk_scan).  This version runs on the CUDA cores (fp32 FFMA).
+//
+// One CTA per (batch, head) walks the chunks in order and keeps the state on
+// chip (fp32 in registers of the state warps), so nothing but x, dt, B, C in
+// and y out touches memory.  Per chunk of Q = 128 steps, four tcgen05 MMAs
+// (bf16 operands, fp32 accumulators in TMEM):
+//   G   = C B^T            [t][s]   A = C, B = B: both K-major (along N)
+//   Y1  = W x              [t][p]   A = W from TMEM, B = x read N-major
+//   U^T = (w B)^T x        [n][p]   A = B scaled by w_s in place, read M-major;
+//                                   B = x, N-major
+//   Y2  = C S_in^T         [t][p]   A = C, B = S_in^T ([n][p] rows) N-major
+// issued in that order as their inputs become ready; only Y2 waits for the
+// carried state, and the state update waits only for U^T.
+// with W[t][s] = G[t][s] exp(cum_t - cum_s) dt_s for s <= t (0 otherwise),
+// plus D on the diagonal (so Y1 carries the skip term D x_t), and
+// w_s = exp(cum_end - cum_s) dt_s.  Then y = Y1 + exp(cum_t) Y2 and
+// S_out^T = exp(cum_end) S_in^T + U^T.  The operands W, w B and S_in are
+// rounded to bf16 for the tensor cores; every sum and the carried state stay
+// fp32.
+//
+// Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-7 decay
+// warps (prefix sums, w B, W; thread i owns step / row i), 8-11 state warps
+// (S rows n, then output rows t; thread i owns TMEM lane i).  Two chunks are
+// in flight: inputs, G/W/U and Y are double-buffered.
 #include <cmath>
 
 #include "kernels.h"
@@ -22,263 +41,467 @@
 namespace gbattn {
 namespace {
 
-constexpr int kQ = 64;       // steps per chunk
-constexpr int kP = 64;       // head dim
-constexpr int kN = 128;      // state dim
-constexpr int kThreads = 256;
+constexpr int kQ = 128;        // steps per chunk (MMA M)
+constexpr int kP = 64;         // head dim
+constexpr int kN = 128;        // state dim
+constexpr int kThreads = 384;
+constexpr uint32_t kAtom = 128 * 128;               // 128 rows x 128 B: 64 bf16 columns, 128-byte swizzle
+constexpr uint32_t kOffC = 0, kOffB = 2 * kAtom, kOffX = 4 * kAtom;
+constexpr uint32_t kStageBytes = 5 * kAtom;         // C, B (two 64-column blocks each), x
+constexpr uint32_t kOffS = 2 * kStageBytes;         // two S_in^T buffers [n][p] bf16
+constexpr uint32_t kOffCtl = kOffS + 2 * kAtom;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// TMEM columns of chunk parity u: G [128u, +128) (W as bf16 pairs over the
+// first 64, U^T over the last 64); Y1 and Y2 at 256 + 128u and + 64.
+__host__ __device__ constexpr uint32_t col_g(int u) { return 128u * u; }
+__host__ __device__ constexpr uint32_t col_y1(int u) { return 256u + 128u * u; }
+__host__ __device__ constexpr uint32_t col_y2(int u) { return 256u + 128u * u + 64u; }
+
+struct SsdCtl {
+    uint64_t full[2];       // TMA: the stage's C, B, x landed
+    uint64_t u_full[2];     // commit after U^T = (w B)^T x (and every earlier MMA)
+    uint64_t mma_done[2];   // commit after the chunk's last MMA (Y2): stage free, Y ready
+    uint64_t g_full[2];     // commit after G = C B^T
+    uint64_t w_full[2];     // decay warps: W written to TMEM
+    uint64_t bp_full[2];    // decay warps: B rows scaled by w_s
+    uint64_t s_ready[2];    // state warps: S_in^T of the chunk in shared memory
+    uint64_t g_free[2];     // state warps: U^T read (G columns reusable)
+    uint64_t y_free[2];     // state warps: Y1, Y2 read
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    float cum_w[kQ], dt_w[kQ], tot_w[4];   // decay warps' prefix of a * log2(e), dt
+    float cum_s[kQ], dt_s[kQ], tot_s[4];   // state warps' copy (same arithmetic)
+};
 
 struct SsdParams {
     const __nv_bfloat16 *x;   // [Bsz][L][H][P]
     const float *dt;          // [Bsz][L][H]
     const float *A;           // [H]
-    const __nv_bfloat16 *Bm;  // [Bsz][L][G][N]
-    const __nv_bfloat16 *Cm;  // [Bsz][L][G][N]
     const float *D;           // [H] or nullptr
     float *y;                 // [Bsz][L][H][P]
     float *S_final;           // [Bsz][H][P][N] or nullptr
-    float *states;            // [Bsz][nchunks][H][P][N]
-    float *dA_end;            // [Bsz][nchunks][H]: cum at the chunk's last step
-    int Bsz, L, H, G, nchunks;
+    int L, H, G, nchunks;
+    int *status;
+    uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
-
-// Inclusive prefix sum of a = dt * A over the chunk's steps into cum[0..len).
-__device__ __forceinline__ void chunk_cumsum(const SsdParams &p, int b, int c, int h, int len, float *cum,
-                                             float *dts)
+// dt of step i of chunk c (0 past the sequence's end).
+__device__ __forceinline__ float load_dt(const SsdParams &p, int b, int h, int c, int i)
 {
-    if (threadIdx.x < 32) {
-        const float Ah = p.A[h];
-        float carry = 0.f;
-        for (int base = 0; base < kQ; base += 32) {
-            const int s = base + threadIdx.x;
-            const float d = s < len ? p.dt[(static_cast<size_t>(b) * p.L + c * kQ + s) * p.H + h] : 0.f;
-            float v = d * Ah;
+    const int row = c * kQ + i;
+    return (c < p.nchunks && row < p.L) ? __ldg(p.dt + (static_cast<size_t>(b) * p.L + row) * p.H + h) : 0.f;
+}
+
+// Inclusive prefix of a_s * log2(e) = dt_s A_h log2(e) over the chunk's steps
+// into cum, dt_s (d, this thread's step) into dts; one thread per step, the 4
+// warps of one group synchronised on named barrier `bar`.
+__device__ __forceinline__ void chunk_prefix(float d, int i, float Al2, float *cum, float *dts, float *tot,
+                                             uint32_t bar)
+{
+    float v = d * Al2;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, v, o);
-                if (threadIdx.x >= o) v += u;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if ((i & 31) >= o) v += u;
+    }
+    if ((i & 31) == 31) tot[i >> 5] = v;
+    named_barrier(bar, 128);
+    float off = 0.f;
+    for (int w = 0; w < (i >> 5); ++w) off += tot[w];
+    cum[i] = off + v;
+    dts[i] = d;
+    named_barrier(bar, 128);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmX, const SsdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    SsdCtl &k = *reinterpret_cast<SsdCtl *>(smem + kOffCtl);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int g = h / (p.H / p.G);
+    const int nch = p.nchunks;
+
+    if (threadIdx.x == 0) {
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(&k.full[u], 1);
+            mbar_init(&k.u_full[u], 1);
+            mbar_init(&k.mma_done[u], 1);
+            mbar_init(&k.g_full[u], 1);
+            mbar_init(&k.w_full[u], 128);
+            mbar_init(&k.bp_full[u], 128);
+            mbar_init(&k.s_ready[u], 128);
+            mbar_init(&k.g_free[u], 128);
+            mbar_init(&k.y_free[u], 128);
+        }
+        mbar_init(&k.drain, 1);
+        k.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(&k.tmem_base, kTmemCols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tbase = k.tmem_base;
+    const WaitCtl ctl{&k.abort, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmC);
+            tma_prefetch_desc(&tmB);
+            tma_prefetch_desc(&tmX);
+            bool ok = true;
+            int c = 0;
+            for (; c < nch; ++c) {
+                const int u = c & 1;
+                if (c >= 2 && !(ok = mbar_wait(&k.mma_done[u], ((c - 2) >> 1) & 1, ctl))) break;
+                uint8_t *st = smem + u * kStageBytes;
+                mbar_arrive_expect_tx(&k.full[u], kStageBytes);
+                const int row = c * kQ;
+                tma_load_4d(st + kOffC, &tmC, &k.full[u], 0, g, row, b);
+                tma_load_4d(st + kOffC + kAtom, &tmC, &k.full[u], 64, g, row, b);
+                tma_load_4d(st + kOffB, &tmB, &k.full[u], 0, g, row, b);
+                tma_load_4d(st + kOffB + kAtom, &tmB, &k.full[u], 64, g, row, b);
+                tma_load_4d(st + kOffX, &tmX, &k.full[u], 0, h, row, b);
             }
-            cum[s] = carry + v;
-            dts[s] = d;
-            carry += __shfl_sync(0xffffffffu, v, 31);
+            if (!ok) {
+                // Aborted: let the loads already issued land before the CTA exits.
+                volatile int no_abort = 0;
+                const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+                for (int i = (c > 2 ? c - 2 : 0); i < c; ++i) mbar_wait(&k.full[i & 1], (i >> 1) & 1, drain);
+            }
+        }
+    } else if (warp == 1) {
+        // =================== tensor-core issuer ===================
+        if (lane == 0) {
+            constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
+            constexpr uint32_t idU = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t sb = smem_u32(smem);
+            int n1 = 0, n3 = 0, n2 = 0, n4 = 0;   // next chunk of each MMA
+            uint64_t t_last = global_timer_ns();
+            uint32_t spins = 0;
+            while (n3 < nch) {   // Y2 is the last MMA of a chunk
+                bool any = false;
+                if (n1 < nch) {
+                    const int c = n1, u = c & 1;
+                    if (mbar_poll(smem_u32(&k.full[u]), (c >> 1) & 1) &&
+                        (c < 2 || mbar_poll(smem_u32(&k.g_free[u]), ((c - 2) >> 1) & 1))) {
+                        tc_fence_after_sync();
+                        const uint32_t st = sb + u * kStageBytes;
+                        const uint64_t ad = smem_desc_sw128(st + kOffC, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(st + kOffB, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kN / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * kAtom + (kk % 4) * 32;
+                            umma_ss(tbase + col_g(u), desc_advance(ad, off), desc_advance(bd, off), idG, kk > 0);
+                        }
+                        umma_commit(&k.g_full[u]);
+                        ++n1;
+                        any = true;
+                    }
+                }
+                if (n2 < n1) {
+                    const int c = n2, u = c & 1;
+                    if (mbar_poll(smem_u32(&k.w_full[u]), (c >> 1) & 1) &&
+                        (c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1))) {
+                        tc_fence_after_sync();
+                        const uint64_t bd = smem_desc_sw128(sb + u * kStageBytes + kOffX, kAtom, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kQ / 16; ++kk)
+                            umma_ts(tbase + col_y1(u), tbase + col_g(u) + kk * 8, desc_advance(bd, kk * 2048), idY,
+                                    kk > 0);
+                        ++n2;
+                        any = true;
+                    }
+                }
+                if (n4 < n2 && n3 >= n4) {   // W read (MMA2 issued); Y2 of the chunk before issued
+                    const int c = n4, u = c & 1;
+                    if (mbar_poll(smem_u32(&k.bp_full[u]), (c >> 1) & 1)) {
+                        tc_fence_after_sync();
+                        const uint32_t st = sb + u * kStageBytes;
+                        const uint64_t ad = smem_desc_sw128(st + kOffB, kAtom, 1024);
+                        const uint64_t bd = smem_desc_sw128(st + kOffX, kAtom, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kQ / 16; ++kk)
+                            umma_ss(tbase + col_g(u) + 64, desc_advance(ad, kk * 2048), desc_advance(bd, kk * 2048),
+                                    idU, kk > 0);
+                        umma_commit(&k.u_full[u]);
+                        ++n4;
+                        any = true;
+                    }
+                }
+                if (n3 < n4) {
+                    const int c = n3, u = c & 1;
+                    if (mbar_poll(smem_u32(&k.s_ready[u]), (c >> 1) & 1) &&
+                        (c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1))) {
+                        tc_fence_after_sync();
+                        const uint32_t st = sb + u * kStageBytes;
+                        const uint64_t ad = smem_desc_sw128(st + kOffC, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sb + kOffS + u * kAtom, kAtom, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kN / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * kAtom + (kk % 4) * 32;
+                            umma_ss(tbase + col_y2(u), desc_advance(ad, off), desc_advance(bd, kk * 2048), idY,
+                                    kk > 0);
+                        }
+                        umma_commit(&k.mma_done[u]);
+                        ++n3;
+                        any = true;
+                    }
+                }
+                if (any) {
+                    t_last = global_timer_ns();
+                    spins = 0;
+                } else if ((++spins & 63u) == 0) {
+                    if (*ctl.abort) break;
+                    if (global_timer_ns() - t_last > p.timeout_ns) {
+                        raise_abort(ctl, kStatusWaitTimeout);
+                        break;
+                    }
+                }
+            }
+            // No tensor-core work may still be in flight when TMEM is freed.
+            umma_commit(&k.drain);
+            volatile int no_abort = 0;
+            const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
+            mbar_wait(&k.drain, 0, drain);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // =================== decay warps: w B and W ===================
+        const int i = threadIdx.x - 128;                      // step s / row t / TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32u << 16;
+        const float Al2 = __ldg(p.A + h) * kLog2e;
+        const float Dh = p.D ? __ldg(p.D + h) : 0.f;
+        float d_next = load_dt(p, b, h, 0, i);
+        for (int c = 0; c < nch; ++c) {
+            const int u = c & 1;
+            const int len = min(kQ, p.L - c * kQ);
+            const float d = d_next;
+            d_next = load_dt(p, b, h, c + 1, i);   // one chunk ahead
+            chunk_prefix(d, i, Al2, k.cum_w, k.dt_w, k.tot_w, 1);
+            // every thread of the group takes the same branch (named barriers follow)
+            if (!barrier_and(1, 128, mbar_wait(&k.g_full[u], (c >> 1) & 1, ctl))) break;
+            tc_fence_after_sync();
+            // B row s = i (both 64-column blocks) times w_s, in place; the
+            // 128-byte swizzle only permutes 16-byte pieces inside the row.
+            {
+                const float cend = k.cum_w[len - 1];
+                const float ws = i < len ? ex2_approx(cend - k.cum_w[i]) * k.dt_w[i] : 0.f;
+                uint8_t *st = smem + u * kStageBytes + kOffB + i * 128;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint4 *r = reinterpret_cast<uint4 *>(st + blk * kAtom);
+                    // visit the pieces in the swizzled order: lanes of a warp then hit
+                    // 8 different bank groups instead of one
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int jj = j ^ (i & 7);
+                        uint4 v = r[jj];
+                        v.x = pack_bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws);
+                        v.y = pack_bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws);
+                        v.z = pack_bf16x2(bf_lo(v.z) * ws, bf_hi(v.z) * ws);
+                        v.w = pack_bf16x2(bf_lo(v.w) * ws, bf_hi(v.w) * ws);
+                        r[jj] = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&k.bp_full[u]);
+            }
+            // W row t = i over G's 128 columns (s), written as bf16 pairs over
+            // the first 64 columns once each 32-column piece has been read.
+            {
+                const int t = i;
+                const float ct = k.cum_w[t];
+                const int t_hi = min(len - 1, (warp - 4) * 32 + 31);   // last valid row of this warp
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[16];
+                    // warp-uniform condition: tcgen05.ld is a warp-collective instruction
+                    if (q * 32 <= t_hi) {
+                        uint32_t gr[32];
+                        tmem_ld_x32(tbase + lane_base + col_g(u) + q * 32, gr);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int s0 = q * 32 + 2 * j, s1 = s0 + 1;
+                            // the skip term D x_t rides on the diagonal: W[t][t] += D
+                            const float f0 =
+                                s0 <= t && t < len
+                                    ? fmaf(__uint_as_float(gr[2 * j]) * ex2_approx(ct - k.cum_w[s0]), k.dt_w[s0],
+                                           s0 == t ? Dh : 0.f)
+                                    : 0.f;
+                            const float f1 =
+                                s1 <= t && t < len
+                                    ? fmaf(__uint_as_float(gr[2 * j + 1]) * ex2_approx(ct - k.cum_w[s1]), k.dt_w[s1],
+                                           s1 == t ? Dh : 0.f)
+                                    : 0.f;
+                            w[j] = pack_bf16x2(f0, f1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w[j] = 0u;
+                    }
+                    tmem_st_x16(tbase + lane_base + col_g(u) + q * 16, w);
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(&k.w_full[u]);
+            }
+        }
+    } else if (warp >= 8) {
+        // =================== state warps: S rows n, then output rows t ===================
+        const int i = threadIdx.x - 256;
+        const uint32_t lane_base = static_cast<uint32_t>(warp - 8) * 32u << 16;
+        const float Al2 = __ldg(p.A + h) * kLog2e;
+        float d_next = load_dt(p, b, h, 0, i);
+        float S[kP];
+#pragma unroll
+        for (int j = 0; j < kP; ++j) S[j] = 0.f;
+        // S_in^T row n = i into buffer u: 64 bf16 = 128 B, 16-byte piece j at
+        // position j ^ (n % 8) (128-byte swizzle, rows n consecutive).
+        auto put_state = [&](int u) {
+            uint8_t *row = smem + kOffS + u * kAtom + i * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 v;
+                v.x = pack_bf16x2(S[8 * j + 0], S[8 * j + 1]);
+                v.y = pack_bf16x2(S[8 * j + 2], S[8 * j + 3]);
+                v.z = pack_bf16x2(S[8 * j + 4], S[8 * j + 5]);
+                v.w = pack_bf16x2(S[8 * j + 6], S[8 * j + 7]);
+                *reinterpret_cast<uint4 *>(row + ((j ^ (i & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&k.s_ready[u]);
+        };
+        put_state(0);
+        for (int c = 0; c < nch; ++c) {
+            const int u = c & 1;
+            const int len = min(kQ, p.L - c * kQ);
+            const float d = d_next;
+            d_next = load_dt(p, b, h, c + 1, i);
+            chunk_prefix(d, i, Al2, k.cum_s, k.dt_s, k.tot_s, 2);
+            if (!barrier_and(2, 128, mbar_wait(&k.u_full[u], (c >> 1) & 1, ctl))) break;
+            tc_fence_after_sync();
+            // S_out^T row n = exp(cum_end) S_in^T row n + U^T row n
+            const float dec = ex2_approx(k.cum_s[len - 1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t r[32];
+                tmem_ld_x32(tbase + lane_base + col_g(u) + 64 + q * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[q * 32 + j] = fmaf(dec, S[q * 32 + j], __uint_as_float(r[j]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&k.g_free[u]);
+            if (c + 1 < nch) put_state((c + 1) & 1);
+            if (!barrier_and(2, 128, mbar_wait(&k.mma_done[u], (c >> 1) & 1, ctl))) break;
+            tc_fence_after_sync();
+            // y row t = i: Y1 (with D x) + exp(cum_t) Y2
+            const int t = i;
+            const float et = ex2_approx(k.cum_s[t]);
+            const size_t grow = (static_cast<size_t>(b) * p.L + static_cast<size_t>(c) * kQ + t) * p.H + h;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t y1[16], y2[16];
+                tmem_ld_x16(tbase + lane_base + col_y1(u) + q * 16, y1);
+                tmem_ld_x16(tbase + lane_base + col_y2(u) + q * 16, y2);
+                if (q == 3) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&k.y_free[u]);
+                }
+                if (t < len) {
+                    float4 *yo = reinterpret_cast<float4 *>(p.y + grow * kP + q * 16);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = fmaf(et, __uint_as_float(y2[4 * j + e]), __uint_as_float(y1[4 * j + e]));
+                        yo[j] = make_float4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+        }
+        if (p.S_final && !*ctl.abort) {
+            float *dst = p.S_final + (static_cast<size_t>(b) * p.H + h) * (kP * kN) + i;
+#pragma unroll
+            for (int j = 0; j < kP; ++j) dst[static_cast<size_t>(j) * kN] = S[j];
         }
     }
-    __syncthreads();
-}
 
-// S_c = sum_s exp(cum_end - cum_s) dt_s x_s B_s^T  ([P][N], one block per (chunk, head, batch)).
-__global__ void __launch_bounds__(kThreads) ssd_chunk_state_kernel(const SsdParams p)
-{
-    extern __shared__ float sm[];
-    float *cum = sm, *dts = sm + kQ;
-    float (*xs)[kP] = reinterpret_cast<float (*)[kP]>(dts + kQ);          // x_s scaled by exp(cum_end - cum_s) dt_s
-    float (*bs)[kN + 4] = reinterpret_cast<float (*)[kN + 4]>(dts + kQ + kQ * kP);
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int g = h / (p.H / p.G);
-    const int len = min(kQ, p.L - c * kQ);
-    chunk_cumsum(p, b, c, h, len, cum, dts);
-    const float cend = cum[len - 1];
-    for (int i = threadIdx.x; i < kQ * kP; i += kThreads) {
-        const int s = i / kP, q = i % kP;
-        float v = 0.f;
-        if (s < len)
-            v = bf(p.x[((static_cast<size_t>(b) * p.L + c * kQ + s) * p.H + h) * kP + q]) * __expf(cend - cum[s]) * dts[s];
-        xs[s][q] = v;
-    }
-    for (int i = threadIdx.x; i < kQ * kN; i += kThreads) {
-        const int s = i / kN, n = i % kN;
-        bs[s][n] = s < len ? bf(p.Bm[((static_cast<size_t>(b) * p.L + c * kQ + s) * p.G + g) * kN + n]) : 0.f;
-    }
+    // ---- teardown (lanes 1-31 of warps 0 and 1 wait here for their lane 0)
+    __syncwarp();
+    tc_fence_before_sync();
     __syncthreads();
-    // thread: rows q = ty*4 .. +4 of P, cols n = tx*8 .. +8 of N (16 x 16 threads)
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[4][8] = {};
-    for (int s = 0; s < len; ++s) {
-        float xv[4], bv[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) xv[i] = xs[s][ty * 4 + i];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) bv[j] = bs[s][tx * 8 + j];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], bv[j], acc[i][j]);
-    }
-    float *dst = p.states + ((static_cast<size_t>(b) * p.nchunks + c) * p.H + h) * (kP * kN);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float4 *o = reinterpret_cast<float4 *>(dst + (ty * 4 + i) * kN + tx * 8);
-        o[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        o[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
-    if (threadIdx.x == 0) p.dA_end[(static_cast<size_t>(b) * p.nchunks + c) * p.H + h] = cend;
-}
-
-// In place over the chunks of each (batch, head): slot c := the state entering
-// chunk c (slot 0 := 0), from the chunk contributions and exp(cum_end).  One
-// thread per state element.
-__global__ void __launch_bounds__(kThreads) ssd_state_pass_kernel(const SsdParams p)
-{
-    const int e = blockIdx.x * kThreads + threadIdx.x;      // element of [P][N]
-    const int h = blockIdx.y, b = blockIdx.z;
-    float carry = 0.f;
-    for (int c = 0; c < p.nchunks; ++c) {
-        float *slot = p.states + ((static_cast<size_t>(b) * p.nchunks + c) * p.H + h) * (kP * kN) + e;
-        const float contrib = *slot;
-        *slot = carry;
-        carry = __expf(p.dA_end[(static_cast<size_t>(b) * p.nchunks + c) * p.H + h]) * carry + contrib;
-    }
-    if (p.S_final) p.S_final[(static_cast<size_t>(b) * p.H + h) * (kP * kN) + e] = carry;
-}
-
-// y of one chunk: intra-chunk products, the entering state, and D x.
-__global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParams p)
-{
-    extern __shared__ float sm[];
-    float *cum = sm;                        // [Q]
-    float *dts = cum + kQ;                  // [Q]
-    float *cs = dts + kQ;                   // [Q][N + 4]
-    float *bs = cs + kQ * (kN + 4);         // [Q][N + 4]
-    float *w = bs + kQ * (kN + 4);          // [Q][Q + 4]: exp(cum_t - cum_s) dt_s (C_t . B_s), s <= t
-    float *xs = w + kQ * (kQ + 4);          // [Q][P]
-    float *st = xs + kQ * kP;               // [P][N + 4]: the entering state
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int g = h / (p.H / p.G);
-    const int len = min(kQ, p.L - c * kQ);
-    chunk_cumsum(p, b, c, h, len, cum, dts);
-    for (int i = threadIdx.x; i < kQ * kN; i += kThreads) {
-        const int s = i / kN, n = i % kN;
-        const size_t src = ((static_cast<size_t>(b) * p.L + c * kQ + s) * p.G + g) * kN + n;
-        cs[s * (kN + 4) + n] = s < len ? bf(p.Cm[src]) : 0.f;
-        bs[s * (kN + 4) + n] = s < len ? bf(p.Bm[src]) : 0.f;
-    }
-    for (int i = threadIdx.x; i < kQ * kP; i += kThreads) {
-        const int s = i / kP, q = i % kP;
-        xs[i] = s < len ? bf(p.x[((static_cast<size_t>(b) * p.L + c * kQ + s) * p.H + h) * kP + q]) : 0.f;
-    }
-    const float *S_in = p.states + ((static_cast<size_t>(b) * p.nchunks + c) * p.H + h) * (kP * kN);
-    for (int i = threadIdx.x; i < kP * kN; i += kThreads) st[(i / kN) * (kN + 4) + i % kN] = S_in[i];
-    __syncthreads();
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    // W[t][s] for t = ty*4..+4, s = tx*4..+4
-    {
-        float acc[4][4] = {};
-        for (int n = 0; n < kN; ++n) {
-            float cv[4], bv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cv[i] = cs[(ty * 4 + i) * (kN + 4) + n];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) bv[j] = bs[(tx * 4 + j) * (kN + 4) + n];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(cv[i], bv[j], acc[i][j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int t = ty * 4 + i, s = tx * 4 + j;
-                w[t * (kQ + 4) + s] = (s <= t && t < len) ? acc[i][j] * __expf(cum[t] - cum[s]) * dts[s] : 0.f;
-            }
-    }
-    __syncthreads();
-    // y[t][q] for t = ty*4..+4, q = tx*4..+4
-    float acc[4][4] = {};
-    for (int s = 0; s < kQ; ++s) {
-        float wv[4], xv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) wv[i] = w[(ty * 4 + i) * (kQ + 4) + s];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) xv[j] = xs[s * kP + tx * 4 + j];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
-    }
-    float acc2[4][4] = {};
-    for (int n = 0; n < kN; ++n) {
-        float cv[4], sv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) cv[i] = cs[(ty * 4 + i) * (kN + 4) + n];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sv[j] = st[(tx * 4 + j) * (kN + 4) + n];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(cv[i], sv[j], acc2[i][j]);
-    }
-    const float Dh = p.D ? p.D[h] : 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = ty * 4 + i;
-        if (t >= len) continue;
-        const float e = __expf(cum[t]);
-        float out[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) out[j] = acc[i][j] + e * acc2[i][j] + Dh * xs[t * kP + tx * 4 + j];
-        float4 *dst = reinterpret_cast<float4 *>(p.y + ((static_cast<size_t>(b) * p.L + c * kQ + t) * p.H + h) * kP +
-                                                 tx * 4);
-        *dst = make_float4(out[0], out[1], out[2], out[3]);
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, kTmemCols);
     }
 }
 
-constexpr size_t kStateSmem = sizeof(float) * (2 * kQ + kQ * kP + kQ * (kN + 4));
-constexpr size_t kScanSmem =
-    sizeof(float) * (2 * kQ + 2 * kQ * (kN + 4) + kQ * (kQ + 4) + kQ * kP + kP * (kN + 4));
+constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(SsdCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 }  // namespace
 
-size_t ssd_workspace_bytes(int Bsz, int L, int H)
-{
-    const size_t nchunks = (static_cast<size_t>(L) + kQ - 1) / kQ;
-    return nchunks * Bsz * H * (static_cast<size_t>(kP) * kN + 1) * sizeof(float);
-}
-
 int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *Bm, const void *Cm, const float *D,
-                    float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, void *workspace,
-                    size_t workspace_bytes, const LaunchEnv &env, std::string &err)
+                    float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, const LaunchEnv &env,
+                    std::string &err)
 {
     if (P != kP || N != kN) {
         err = "ssd_scan: supports P = 64, N = 128";
         return 2;
     }
-    if (workspace_bytes < ssd_workspace_bytes(Bsz, L, H)) {
-        err = "ssd_scan: workspace too small";
-        return 4;
-    }
+    CUtensorMap tc, tb, tx;
+    const uint64_t bc_dims[4] = {static_cast<uint64_t>(kN), static_cast<uint64_t>(G), static_cast<uint64_t>(L),
+                                 static_cast<uint64_t>(Bsz)};
+    const uint64_t bc_strides[3] = {kN * 2ull, static_cast<uint64_t>(G) * kN * 2,
+                                    static_cast<uint64_t>(L) * G * kN * 2};
+    const uint64_t x_dims[4] = {static_cast<uint64_t>(kP), static_cast<uint64_t>(H), static_cast<uint64_t>(L),
+                                static_cast<uint64_t>(Bsz)};
+    const uint64_t x_strides[3] = {kP * 2ull, static_cast<uint64_t>(H) * kP * 2,
+                                   static_cast<uint64_t>(L) * H * kP * 2};
+    const uint32_t box[4] = {64, 1, kQ, 1};
+    if (!make_tma_bf16_4d(tc, Cm, bc_dims, bc_strides, box, err) ||
+        !make_tma_bf16_4d(tb, Bm, bc_dims, bc_strides, box, err) ||
+        !make_tma_bf16_4d(tx, x, x_dims, x_strides, box, err))
+        return 5;
     SsdParams p;
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.dt = dt;
     p.A = A;
-    p.Bm = static_cast<const __nv_bfloat16 *>(Bm);
-    p.Cm = static_cast<const __nv_bfloat16 *>(Cm);
     p.D = D;
     p.y = y;
     p.S_final = S_final;
-    p.Bsz = Bsz;
     p.L = L;
     p.H = H;
     p.G = G;
     p.nchunks = (L + kQ - 1) / kQ;
-    p.states = static_cast<float *>(workspace);
-    p.dA_end = p.states + static_cast<size_t>(p.nchunks) * Bsz * H * kP * kN;
-    const dim3 grid(p.nchunks, H, Bsz);
+    p.status = env.status;
+    p.timeout_ns = env.timeout_ns;
     static bool configured = false;
     cudaError_t e = cudaSuccess;
     if (!configured) {
-        e = cudaFuncSetAttribute(ssd_chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kStateSmem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ssd_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kScanSmem));
+        e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
         configured = e == cudaSuccess;
     }
     if (e == cudaSuccess) {
-        ssd_chunk_state_kernel<<<grid, kThreads, kStateSmem, env.stream>>>(p);
-        ssd_state_pass_kernel<<<dim3(kP * kN / kThreads, H, Bsz), kThreads, 0, env.stream>>>(p);
-        ssd_chunk_scan_kernel<<<grid, kThreads, kScanSmem, env.stream>>>(p);
+        ssd_scan_kernel<<<dim3(H, Bsz), kThreads, kSmemBytes, env.stream>>>(tc, tb, tx, p);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {
