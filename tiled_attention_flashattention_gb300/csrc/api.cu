@@ -126,8 +126,8 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
     return true;
 }
 
-bool make_tma_bf16_4d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[4],
-                      const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
+bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
+                 const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
 {
     EncodeFn encode = tensor_map_encoder();
     if (!encode) {
@@ -138,7 +138,8 @@ bool make_tma_bf16_4d(CUtensorMap &desc, const void *base, const uint64_t (&dims
     const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
     const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
-    CUresult r = encode(&desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), d, st, bx, estride,
+    CUresult r = encode(&desc, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        const_cast<void *>(base), d, st, bx, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {

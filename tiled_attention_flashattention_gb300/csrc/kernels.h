@@ -68,9 +68,9 @@ int launch_selftest_umma(const void *A, const void *B, const void *P, const void
 // Returns false and fills err on failure.
 bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t outer, uint32_t box_rows, std::string &err);
-// 4-D bf16 tensor map, 128-byte swizzle; dims innermost first, strides in bytes
-// of dims 1..3, box in elements (box[0] * 2 bytes = 128).
-bool make_tma_bf16_4d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[4],
-                      const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err);
+// 4-D bf16 (f32 = false) or fp32 tensor map, 128-byte swizzle; dims innermost
+// first, strides in bytes of dims 1..3, box in elements (inner box 128 bytes).
+bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
+                 const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err);
 
 }  // namespace gbattn

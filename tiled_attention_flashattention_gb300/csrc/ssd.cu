@@ -29,10 +29,11 @@
 // rounded to bf16 for the tensor cores; every sum and the carried state stay
 // fp32.
 //
-// Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4-7 decay
-// warps (prefix sums, w B, W; thread i owns step / row i), 8-11 state warps
-// (S rows n, then output rows t; thread i owns TMEM lane i).  Two chunks are
-// in flight: inputs, G/W/U and Y are double-buffered.
+// Warps: 0 TMA producer, 1 MMA issuer, 2-3 B warps (TMEM allocation, then
+// w B in place; thread i owns steps i and i + 64), 4-7 decay warps (W; thread
+// i owns row i), 8-11 state warps (S rows n, then output rows t through a
+// swizzled staging slice and TMA stores; thread i owns TMEM lane i).  Two
+// chunks are in flight: inputs, G/W/U and Y are double-buffered.
 #include <cmath>
 
 #include "kernels.h"
@@ -49,7 +50,10 @@ constexpr uint32_t kAtom = 128 * 128;               // 128 rows x 128 B: 64 bf16
 constexpr uint32_t kOffC = 0, kOffB = 2 * kAtom, kOffX = 4 * kAtom;
 constexpr uint32_t kStageBytes = 5 * kAtom;         // C, B (two 64-column blocks each), x
 constexpr uint32_t kOffS = 2 * kStageBytes;         // two S_in^T buffers [n][p] bf16
-constexpr uint32_t kOffCtl = kOffS + 2 * kAtom;
+constexpr uint32_t kOffY = kOffS + 2 * kAtom;       // y staging: 4 slices of 32 rows x 32 fp32 (128 B rows)
+constexpr uint32_t kYSlice = 32 * 128;
+constexpr uint32_t kOffCtl = kOffY + 4 * kYSlice;
+constexpr float kSafeSpan = 96.f;                   // largest in-block decay (log2) of the factored W
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -65,7 +69,7 @@ struct SsdCtl {
     uint64_t mma_done[2];   // commit after the chunk's last MMA (Y2): stage free, Y ready
     uint64_t g_full[2];     // commit after G = C B^T
     uint64_t w_full[2];     // decay warps: W written to TMEM
-    uint64_t bp_full[2];    // decay warps: B rows scaled by w_s
+    uint64_t bp_full[2];    // B warps: B rows scaled by w_s
     uint64_t s_ready[2];    // state warps: S_in^T of the chunk in shared memory
     uint64_t g_free[2];     // state warps: U^T read (G columns reusable)
     uint64_t y_free[2];     // state warps: Y1, Y2 read
@@ -73,7 +77,9 @@ struct SsdCtl {
     uint32_t tmem_base;
     int abort;
     float cum_w[kQ], dt_w[kQ], tot_w[4];   // decay warps' prefix of a * log2(e), dt
+    alignas(16) float col_w[kQ];           // decay warps: 2^(cum at block start - cum_s) dt_s
     float cum_s[kQ], dt_s[kQ], tot_s[4];   // state warps' copy (same arithmetic)
+    float tot_b[2][4];                     // B warps: 32-step group totals (by chunk parity)
 };
 
 struct SsdParams {
@@ -121,7 +127,8 @@ __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmX, const SsdParams p)
+                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                    const SsdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&k.mma_done[u], 1);
             mbar_init(&k.g_full[u], 1);
             mbar_init(&k.w_full[u], 128);
-            mbar_init(&k.bp_full[u], 128);
+            mbar_init(&k.bp_full[u], 64);
             mbar_init(&k.s_ready[u], 128);
             mbar_init(&k.g_free[u], 128);
             mbar_init(&k.y_free[u], 128);
@@ -164,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmC);
             tma_prefetch_desc(&tmB);
             tma_prefetch_desc(&tmX);
+            tma_prefetch_desc(&tmY);
             bool ok = true;
             int c = 0;
             for (; c < nch; ++c) {
@@ -281,8 +289,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
             mbar_wait(&k.drain, 0, drain);
         }
+    } else if (warp == 2 || warp == 3) {
+        // =================== B warps: rows s of B times w_s ===================
+        const int i = threadIdx.x - 64;                       // steps i and i + 64
+        const float Al2 = __ldg(p.A + h) * kLog2e;
+        float d0n = load_dt(p, b, h, 0, i), d1n = load_dt(p, b, h, 0, i + 64);
+        for (int c = 0; c < nch; ++c) {
+            const int u = c & 1;
+            const float d0 = d0n, d1 = d1n;
+            d0n = load_dt(p, b, h, c + 1, i);
+            d1n = load_dt(p, b, h, c + 1, i + 64);
+            // prefix over the chunk: groups of 32 steps (warp 2: 0-31, 64-95; warp 3: 32-63, 96-127)
+            float v0 = d0 * Al2, v1 = d1 * Al2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float a0 = __shfl_up_sync(0xffffffffu, v0, o), a1 = __shfl_up_sync(0xffffffffu, v1, o);
+                if (lane >= o) {
+                    v0 += a0;
+                    v1 += a1;
+                }
+            }
+            if (lane == 31) {
+                k.tot_b[u][warp - 2] = v0;
+                k.tot_b[u][warp] = v1;
+            }
+            named_barrier(3, 64);
+            const float t0 = k.tot_b[u][0], t1 = k.tot_b[u][1], t2 = k.tot_b[u][2], t3 = k.tot_b[u][3];
+            const float cend = ((t0 + t1) + t2) + t3;
+            const float c0 = (warp == 2 ? 0.f : t0) + v0;
+            const float c1 = (warp == 2 ? t0 + t1 : (t0 + t1) + t2) + v1;
+            // every thread of the group takes the same branch (named barriers follow)
+            if (!barrier_and(3, 64, mbar_wait(&k.g_full[u], (c >> 1) & 1, ctl))) break;
+            // rows s = i and i + 64 (both 64-column blocks) times w_s, in place; the
+            // 128-byte swizzle only permutes 16-byte pieces inside a row, and
+            // visiting them in the swizzled order spreads a warp over all banks.
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int srow = i + 64 * r;
+                const float ws = (r ? d1 : d0) == 0.f ? 0.f : ex2_approx(cend - (r ? c1 : c0)) * (r ? d1 : d0);
+                uint8_t *st = smem + u * kStageBytes + kOffB + srow * 128;
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint4 *row = reinterpret_cast<uint4 *>(st + blk * kAtom);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int jj = j ^ (srow & 7);
+                        uint4 v = row[jj];
+                        v.x = pack_bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws);
+                        v.y = pack_bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws);
+                        v.z = pack_bf16x2(bf_lo(v.z) * ws, bf_hi(v.z) * ws);
+                        v.w = pack_bf16x2(bf_lo(v.w) * ws, bf_hi(v.w) * ws);
+                        row[jj] = v;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&k.bp_full[u]);
+        }
     } else if (warp >= 4 && warp < 8) {
-        // =================== decay warps: w B and W ===================
+        // =================== decay warps: W ===================
         const int i = threadIdx.x - 128;                      // step s / row t / TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32u << 16;
         const float Al2 = __ldg(p.A + h) * kLog2e;
@@ -294,73 +359,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float d = d_next;
             d_next = load_dt(p, b, h, c + 1, i);   // one chunk ahead
             chunk_prefix(d, i, Al2, k.cum_w, k.dt_w, k.tot_w, 1);
-            // every thread of the group takes the same branch (named barriers follow)
+            // column factors of the factored weights: 2^(cum_{32q} - cum_s) dt_s, s in block q
+            const float span_i = k.cum_w[i & ~31] - k.cum_w[i];
+            k.col_w[i] = fabsf(span_i) <= kSafeSpan ? ex2_approx(span_i) * k.dt_w[i] : 0.f;
             if (!barrier_and(1, 128, mbar_wait(&k.g_full[u], (c >> 1) & 1, ctl))) break;
             tc_fence_after_sync();
-            // B row s = i (both 64-column blocks) times w_s, in place; the
-            // 128-byte swizzle only permutes 16-byte pieces inside the row.
-            {
-                const float cend = k.cum_w[len - 1];
-                const float ws = i < len ? ex2_approx(cend - k.cum_w[i]) * k.dt_w[i] : 0.f;
-                uint8_t *st = smem + u * kStageBytes + kOffB + i * 128;
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    uint4 *r = reinterpret_cast<uint4 *>(st + blk * kAtom);
-                    // visit the pieces in the swizzled order: lanes of a warp then hit
-                    // 8 different bank groups instead of one
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jj = j ^ (i & 7);
-                        uint4 v = r[jj];
-                        v.x = pack_bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws);
-                        v.y = pack_bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws);
-                        v.z = pack_bf16x2(bf_lo(v.z) * ws, bf_hi(v.z) * ws);
-                        v.w = pack_bf16x2(bf_lo(v.w) * ws, bf_hi(v.w) * ws);
-                        r[jj] = v;
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&k.bp_full[u]);
-            }
             // W row t = i over G's 128 columns (s), written as bf16 pairs over
             // the first 64 columns once each 32-column piece has been read.
-            {
-                const int t = i;
-                const float ct = k.cum_w[t];
-                const int t_hi = min(len - 1, (warp - 4) * 32 + 31);   // last valid row of this warp
+            // In block q, W[t][s] = G[t][s] 2^(cum_t - cum_{32q}) col_s, unless
+            // the block's decay span is too large for col_s (then 2^(cum_t -
+            // cum_s) dt_s directly); the skip term D rides on the diagonal.
+            const int t = i;
+            const float ct = k.cum_w[t];
+            const int t_hi = min(len - 1, (warp - 4) * 32 + 31);   // last valid row of this warp
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w[16];
-                    // warp-uniform condition: tcgen05.ld is a warp-collective instruction
-                    if (q * 32 <= t_hi) {
-                        uint32_t gr[32];
-                        tmem_ld_x32(tbase + lane_base + col_g(u) + q * 32, gr);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[16];
+                // warp-uniform condition: tcgen05.ld is a warp-collective instruction
+                if (q * 32 <= t_hi) {
+                    uint32_t gr[32];
+                    tmem_ld_x32(tbase + lane_base + col_g(u) + q * 32, gr);
+                    const float m = k.cum_w[q * 32];
+                    // a = dt A has one sign per head, so the block's span is at its ends (uniform)
+                    const bool safe = fabsf(m - k.cum_w[min(q * 32 + 31, len - 1)]) <= kSafeSpan;
+                    const bool row_ok = t < len;
+                    if (safe) {
+                        const float rt = ex2_approx(ct - m);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int s0 = q * 32 + 2 * j, s1 = s0 + 1;
-                            // the skip term D x_t rides on the diagonal: W[t][t] += D
+                            const float2 cf = *reinterpret_cast<const float2 *>(&k.col_w[s0]);
+                            float f0 = __uint_as_float(gr[2 * j]) * cf.x * rt;
+                            float f1 = __uint_as_float(gr[2 * j + 1]) * cf.y * rt;
+                            f0 = (s0 < t && row_ok) ? f0 : (s0 == t && row_ok ? f0 + Dh : 0.f);
+                            f1 = (s1 < t && row_ok) ? f1 : (s1 == t && row_ok ? f1 + Dh : 0.f);
+                            w[j] = pack_bf16x2(f0, f1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int s0 = q * 32 + 2 * j, s1 = s0 + 1;
                             const float f0 =
-                                s0 <= t && t < len
+                                s0 <= t && row_ok
                                     ? fmaf(__uint_as_float(gr[2 * j]) * ex2_approx(ct - k.cum_w[s0]), k.dt_w[s0],
                                            s0 == t ? Dh : 0.f)
                                     : 0.f;
                             const float f1 =
-                                s1 <= t && t < len
+                                s1 <= t && row_ok
                                     ? fmaf(__uint_as_float(gr[2 * j + 1]) * ex2_approx(ct - k.cum_w[s1]), k.dt_w[s1],
                                            s1 == t ? Dh : 0.f)
                                     : 0.f;
                             w[j] = pack_bf16x2(f0, f1);
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) w[j] = 0u;
                     }
-                    tmem_st_x16(tbase + lane_base + col_g(u) + q * 16, w);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w[j] = 0u;
                 }
-                tmem_st_wait();
-                tc_fence_before_sync();
-                mbar_arrive(&k.w_full[u]);
+                tmem_st_x16(tbase + lane_base + col_g(u) + q * 16, w);
             }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&k.w_full[u]);
         }
     } else if (warp >= 8) {
         // =================== state warps: S rows n, then output rows t ===================
@@ -410,32 +470,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c + 1 < nch) put_state((c + 1) & 1);
             if (!barrier_and(2, 128, mbar_wait(&k.mma_done[u], (c >> 1) & 1, ctl))) break;
             tc_fence_after_sync();
-            // y row t = i: Y1 (with D x) + exp(cum_t) Y2
+            // y rows of this warp: Y1 (with D x) + exp(cum_t) Y2, two 32-column
+            // halves, each staged as 32 rows x 128 B (128-byte swizzle) and
+            // written by one TMA store (rows past the sequence are clipped).
             const int t = i;
             const float et = ex2_approx(k.cum_s[t]);
-            const size_t grow = (static_cast<size_t>(b) * p.L + static_cast<size_t>(c) * kQ + t) * p.H + h;
+            uint8_t *slice = smem + kOffY + (warp - 8) * kYSlice;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t y1[16], y2[16];
-                tmem_ld_x16(tbase + lane_base + col_y1(u) + q * 16, y1);
-                tmem_ld_x16(tbase + lane_base + col_y2(u) + q * 16, y2);
-                if (q == 3) {
-                    tc_fence_before_sync();
-                    mbar_arrive(&k.y_free[u]);
-                }
-                if (t < len) {
-                    float4 *yo = reinterpret_cast<float4 *>(p.y + grow * kP + q * 16);
+            for (int hh = 0; hh < 2; ++hh) {
+                if (lane == 0) bulk_wait_read_all();   // the slice's previous store has read it
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            o[e] = fmaf(et, __uint_as_float(y2[4 * j + e]), __uint_as_float(y1[4 * j + e]));
-                        yo[j] = make_float4(o[0], o[1], o[2], o[3]);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int col = hh * 32 + q2 * 16;
+                    uint32_t y1[16], y2[16];
+                    tmem_ld_x16(tbase + lane_base + col_y1(u) + col, y1);
+                    tmem_ld_x16(tbase + lane_base + col_y2(u) + col, y2);
+                    if (hh == 1 && q2 == 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&k.y_free[u]);
                     }
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        float4 o;
+                        o.x = fmaf(et, __uint_as_float(y2[4 * jj + 0]), __uint_as_float(y1[4 * jj + 0]));
+                        o.y = fmaf(et, __uint_as_float(y2[4 * jj + 1]), __uint_as_float(y1[4 * jj + 1]));
+                        o.z = fmaf(et, __uint_as_float(y2[4 * jj + 2]), __uint_as_float(y1[4 * jj + 2]));
+                        o.w = fmaf(et, __uint_as_float(y2[4 * jj + 3]), __uint_as_float(y1[4 * jj + 3]));
+                        const int piece = q2 * 4 + jj;
+                        *reinterpret_cast<float4 *>(slice + lane * 128 + ((piece ^ (lane & 7)) << 4)) = o;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&tmY, slice, hh * 32, h, c * kQ + (warp - 8) * 32, b);
+                    bulk_commit_group();
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();   // stores complete before the CTA's shared memory goes away
         if (p.S_final && !*ctl.abort) {
             float *dst = p.S_final + (static_cast<size_t>(b) * p.H + h) * (kP * kN) + i;
 #pragma unroll
@@ -466,7 +540,7 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
         err = "ssd_scan: supports P = 64, N = 128";
         return 2;
     }
-    CUtensorMap tc, tb, tx;
+    CUtensorMap tc, tb, tx, ty;
     const uint64_t bc_dims[4] = {static_cast<uint64_t>(kN), static_cast<uint64_t>(G), static_cast<uint64_t>(L),
                                  static_cast<uint64_t>(Bsz)};
     const uint64_t bc_strides[3] = {kN * 2ull, static_cast<uint64_t>(G) * kN * 2,
@@ -475,10 +549,14 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
                                 static_cast<uint64_t>(Bsz)};
     const uint64_t x_strides[3] = {kP * 2ull, static_cast<uint64_t>(H) * kP * 2,
                                    static_cast<uint64_t>(L) * H * kP * 2};
+    const uint64_t y_strides[3] = {kP * 4ull, static_cast<uint64_t>(H) * kP * 4,
+                                   static_cast<uint64_t>(L) * H * kP * 4};
     const uint32_t box[4] = {64, 1, kQ, 1};
-    if (!make_tma_bf16_4d(tc, Cm, bc_dims, bc_strides, box, err) ||
-        !make_tma_bf16_4d(tb, Bm, bc_dims, bc_strides, box, err) ||
-        !make_tma_bf16_4d(tx, x, x_dims, x_strides, box, err))
+    const uint32_t ybox[4] = {32, 1, 32, 1};
+    if (!make_tma_4d(tc, false, Cm, bc_dims, bc_strides, box, err) ||
+        !make_tma_4d(tb, false, Bm, bc_dims, bc_strides, box, err) ||
+        !make_tma_4d(tx, false, x, x_dims, x_strides, box, err) ||
+        !make_tma_4d(ty, true, y, x_dims, y_strides, ybox, err))
         return 5;
     SsdParams p;
     p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -501,7 +579,7 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
         configured = e == cudaSuccess;
     }
     if (e == cudaSuccess) {
-        ssd_scan_kernel<<<dim3(H, Bsz), kThreads, kSmemBytes, env.stream>>>(tc, tb, tx, p);
+        ssd_scan_kernel<<<dim3(H, Bsz), kThreads, kSmemBytes, env.stream>>>(tc, tb, tx, ty, p);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {
