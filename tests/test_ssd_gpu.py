@@ -4,13 +4,14 @@ several B/C groups, no D term, the final state, degenerate dt and A, and a
 sampled Mamba-2-sized case.
 
 Tolerance, from the arithmetic: the kernel takes the same bf16 inputs and sums
-in fp32, but three operands of its tensor-core products are rounded to bf16
-(relative error at most 2^-9 each): the chunk weights exp(cum_t - cum_s) dt_s
-(C_t . B_s), the decayed rows exp(cum_end - cum_s) dt_s B_s, and the carried
-state.  Every term of y is bounded by the matching term of the same recurrence
-run on |x|, |B|, |C|, |D| (y_abs, by the oracle), and each term carries at
-most two of those roundings, so |y - y_ref| <= 2^-8 y_abs plus fp32 noise; the
-test allows 2^-7 y_abs + 1e-6 (the same for the final state against S_abs).
+in fp32, but operands of its tensor-core products are rounded to bf16
+(relative error at most 2^-9 per rounding): the chunk weights exp(cum_t -
+cum_s) dt_s (C_t . B_s) once, the decayed rows exp(cum_end - cum_s) dt_s B_s
+twice (the factor, then the product), and the carried state once.  Every term
+of y is bounded by the matching term of the same recurrence run on |x|, |B|,
+|C|, |D| (y_abs, by the oracle), and each term carries at most three of those
+roundings, so |y - y_ref| <= 3 * 2^-9 y_abs plus fp32 noise; the test allows
+2^-7 y_abs + 1e-6 (the same for the final state against S_abs).
 A dropped term, a wrong sign or a shifted decay moves y by a sizeable part of
 y_abs and fails it."""
 import numpy as np

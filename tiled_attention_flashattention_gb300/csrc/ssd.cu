@@ -20,17 +20,18 @@
 //   U^T = (w B)^T x        [n][p]   A = B scaled by w_s in place, read M-major;
 //                                   B = x, N-major
 //   Y2  = C S_in^T         [t][p]   A = C, B = S_in^T ([n][p] rows) N-major
-// issued in that order as their inputs become ready; only Y2 waits for the
-// carried state, and the state update waits only for U^T.
+// each issued as soon as its inputs are ready; only Y2 waits for the carried
+// state, and the state update waits only for U^T.
 // with W[t][s] = G[t][s] exp(cum_t - cum_s) dt_s for s <= t (0 otherwise),
 // plus D on the diagonal (so Y1 carries the skip term D x_t), and
 // w_s = exp(cum_end - cum_s) dt_s.  Then y = Y1 + exp(cum_t) Y2 and
 // S_out^T = exp(cum_end) S_in^T + U^T.  The operands W, w B and S_in are
-// rounded to bf16 for the tensor cores; every sum and the carried state stay
-// fp32.
+// rounded to bf16 for the tensor cores (w B as the bf16 product of B and w
+// rounded to bf16); every sum and the carried state stay fp32.
 //
-// Warps: 0 TMA producer, 1 MMA issuer, 2-3 B warps (TMEM allocation, then
-// w B in place; thread i owns steps i and i + 64), 4-7 decay warps (W; thread
+// Warps: 0-1 B warps (w B in place for rows 0-63; they run their own prefix
+// over the chunk), 2 TMEM allocator and MMA issuer, 3 TMA producer, 4-7 decay
+// warps (4-5 also scale B rows 64-127; then W; thread
 // i owns row i), 8-11 state warps (S rows n, then output rows t through a
 // swizzled staging slice and TMA stores; thread i owns TMEM lane i).  Two
 // chunks are in flight: inputs, G/W/U and Y are double-buffered.
@@ -69,7 +70,7 @@ struct SsdCtl {
     uint64_t mma_done[2];   // commit after the chunk's last MMA (Y2): stage free, Y ready
     uint64_t g_full[2];     // commit after G = C B^T
     uint64_t w_full[2];     // decay warps: W written to TMEM
-    uint64_t bp_full[2];    // B warps: B rows scaled by w_s
+    uint64_t bp_full[2];    // B warps (rows 0-63), decay warps 4-5 (rows 64-127): B rows scaled by w_s
     uint64_t s_ready[2];    // state warps: S_in^T of the chunk in shared memory
     uint64_t g_free[2];     // state warps: U^T read (G columns reusable)
     uint64_t y_free[2];     // state warps: Y1, Y2 read
@@ -122,8 +123,37 @@ __device__ __forceinline__ void chunk_prefix(float d, int i, float Al2, float *c
     named_barrier(bar, 128);
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// Two bf16 products, each rounded once to bf16.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+
+// Row s of the stage's B (both 64-column blocks) times w (bf16), in place.
+// The 128-byte swizzle only permutes 16-byte pieces inside a row; visiting
+// them in the swizzled order spreads a warp over all banks.
+__device__ __forceinline__ void scale_b_row(uint8_t *stage_b, int srow, float w)
+{
+    const uint32_t w2 = pack_bf16x2(w, w);
+    uint8_t *st = stage_b + srow * 128;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        uint4 *row = reinterpret_cast<uint4 *>(st + blk * kAtom);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int jj = j ^ (srow & 7);
+            uint4 v = row[jj];
+            v.x = mul_bf16x2(v.x, w2);
+            v.y = mul_bf16x2(v.y, w2);
+            v.z = mul_bf16x2(v.z, w2);
+            v.w = mul_bf16x2(v.w, w2);
+            row[jj] = v;
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
@@ -146,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&k.mma_done[u], 1);
             mbar_init(&k.g_full[u], 1);
             mbar_init(&k.w_full[u], 128);
-            mbar_init(&k.bp_full[u], 64);
+            mbar_init(&k.bp_full[u], 128);
             mbar_init(&k.s_ready[u], 128);
             mbar_init(&k.g_free[u], 128);
             mbar_init(&k.y_free[u], 128);
@@ -165,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = k.tmem_base;
     const WaitCtl ctl{&k.abort, p.status, p.timeout_ns};
 
-    if (warp == 0) {
+    if (warp == 3) {
         // =================== TMA producer ===================
         if (lane == 0) {
             tma_prefetch_desc(&tmC);
@@ -185,6 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(st + kOffB, &tmB, &k.full[u], 0, g, row, b);
                 tma_load_4d(st + kOffB + kAtom, &tmB, &k.full[u], 64, g, row, b);
                 tma_load_4d(st + kOffX, &tmX, &k.full[u], 0, h, row, b);
+                // x of this head comes from HBM: ask for it two chunks ahead, so the
+                // load that refills this stage finds it in L2 (C and B are shared by
+                // the heads of the group and mostly there already)
+                if (c + 2 < nch) tma_prefetch_l2_4d(&tmX, 0, h, row + 2 * kQ, b);
             }
             if (!ok) {
                 // Aborted: let the loads already issued land before the CTA exits.
@@ -193,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = (c > 2 ? c - 2 : 0); i < c; ++i) mbar_wait(&k.full[i & 1], (i >> 1) & 1, drain);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 2) {
         // =================== tensor-core issuer ===================
         if (lane == 0) {
             constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
@@ -201,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idU = idesc_bf16_f32(128, 64, true, true);
             const uint32_t sb = smem_u32(smem);
             int n1 = 0, n3 = 0, n2 = 0, n4 = 0;   // next chunk of each MMA
+            int n_done = 0;                      // chunks whose completion barrier is committed
             uint64_t t_last = global_timer_ns();
             uint32_t spins = 0;
-            while (n3 < nch) {   // Y2 is the last MMA of a chunk
+            while (n_done < nch) {
                 bool any = false;
                 if (n1 < nch) {
                     const int c = n1, u = c & 1;
@@ -237,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         any = true;
                     }
                 }
-                if (n4 < n2 && n3 >= n4) {   // W read (MMA2 issued); Y2 of the chunk before issued
+                if (n4 < n2 && n3 >= n4) {   // W read (MMA2 issued); Y2 of the previous chunk issued
                     const int c = n4, u = c & 1;
                     if (mbar_poll(smem_u32(&k.bp_full[u]), (c >> 1) & 1)) {
                         tc_fence_after_sync();
@@ -253,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         any = true;
                     }
                 }
-                if (n3 < n4) {
+                if (n3 < n1) {
                     const int c = n3, u = c & 1;
                     if (mbar_poll(smem_u32(&k.s_ready[u]), (c >> 1) & 1) &&
                         (c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1))) {
@@ -267,10 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_ss(tbase + col_y2(u), desc_advance(ad, off), desc_advance(bd, kk * 2048), idY,
                                     kk > 0);
                         }
-                        umma_commit(&k.mma_done[u]);
                         ++n3;
                         any = true;
                     }
+                }
+                // a chunk is done once its Y1, Y2 and U^T products are all issued
+                while (n_done < min(n2, min(n3, n4))) {
+                    umma_commit(&k.mma_done[n_done & 1]);
+                    ++n_done;
                 }
                 if (any) {
                     t_last = global_timer_ns();
@@ -289,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
             mbar_wait(&k.drain, 0, drain);
         }
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp < 2) {
         // =================== B warps: rows s of B times w_s ===================
-        const int i = threadIdx.x - 64;                       // steps i and i + 64
+        const int i = threadIdx.x;                            // steps i and i + 64
         const float Al2 = __ldg(p.A + h) * kLog2e;
-        float d0n = load_dt(p, b, h, 0, i), d1n = load_dt(p, b, h, 0, i + 64);
+        float d0n = load_dt(p, b, h, 0, i), d1n = load_dt(p, b, h, 0, i + 64);   // steps i, i + 64
         for (int c = 0; c < nch; ++c) {
             const int u = c & 1;
             const float d0 = d0n, d1 = d1n;
             d0n = load_dt(p, b, h, c + 1, i);
             d1n = load_dt(p, b, h, c + 1, i + 64);
-            // prefix over the chunk: groups of 32 steps (warp 2: 0-31, 64-95; warp 3: 32-63, 96-127)
+            // prefix over the chunk: groups of 32 steps (warp 0: 0-31, 64-95; warp 1: 32-63, 96-127)
             float v0 = d0 * Al2, v1 = d1 * Al2;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -310,39 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (lane == 31) {
-                k.tot_b[u][warp - 2] = v0;
-                k.tot_b[u][warp] = v1;
+                k.tot_b[u][warp] = v0;
+                k.tot_b[u][warp + 2] = v1;
             }
             named_barrier(3, 64);
             const float t0 = k.tot_b[u][0], t1 = k.tot_b[u][1], t2 = k.tot_b[u][2], t3 = k.tot_b[u][3];
             const float cend = ((t0 + t1) + t2) + t3;
-            const float c0 = (warp == 2 ? 0.f : t0) + v0;
-            const float c1 = (warp == 2 ? t0 + t1 : (t0 + t1) + t2) + v1;
+            const float c0 = (warp == 0 ? 0.f : t0) + v0;
             // every thread of the group takes the same branch (named barriers follow)
             if (!barrier_and(3, 64, mbar_wait(&k.g_full[u], (c >> 1) & 1, ctl))) break;
-            // rows s = i and i + 64 (both 64-column blocks) times w_s, in place; the
-            // 128-byte swizzle only permutes 16-byte pieces inside a row, and
-            // visiting them in the swizzled order spreads a warp over all banks.
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int srow = i + 64 * r;
-                const float ws = (r ? d1 : d0) == 0.f ? 0.f : ex2_approx(cend - (r ? c1 : c0)) * (r ? d1 : d0);
-                uint8_t *st = smem + u * kStageBytes + kOffB + srow * 128;
-#pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    uint4 *row = reinterpret_cast<uint4 *>(st + blk * kAtom);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jj = j ^ (srow & 7);
-                        uint4 v = row[jj];
-                        v.x = pack_bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws);
-                        v.y = pack_bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws);
-                        v.z = pack_bf16x2(bf_lo(v.z) * ws, bf_hi(v.z) * ws);
-                        v.w = pack_bf16x2(bf_lo(v.w) * ws, bf_hi(v.w) * ws);
-                        row[jj] = v;
-                    }
-                }
-            }
+            // rows s = i < 64 (rows 64-127 are scaled by decay warps 4-5)
+            scale_b_row(smem + u * kStageBytes + kOffB, i, d0 == 0.f ? 0.f : ex2_approx(cend - c0) * d0);
             fence_proxy_async_smem();
             mbar_arrive(&k.bp_full[u]);
         }
@@ -364,6 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             k.col_w[i] = fabsf(span_i) <= kSafeSpan ? ex2_approx(span_i) * k.dt_w[i] : 0.f;
             if (!barrier_and(1, 128, mbar_wait(&k.g_full[u], (c >> 1) & 1, ctl))) break;
             tc_fence_after_sync();
+            if (warp < 6) {
+                // B rows 64-127 (their W rows are the light ones)
+                const int srow = i + 64;
+                scale_b_row(smem + u * kStageBytes + kOffB, srow,
+                            ex2_approx(k.cum_w[len - 1] - k.cum_w[srow]) * k.dt_w[srow]);
+                fence_proxy_async_smem();
+                mbar_arrive(&k.bp_full[u]);
+            }
             // W row t = i over G's 128 columns (s), written as bf16 pairs over
             // the first 64 columns once each 32-column piece has been read.
             // In block q, W[t][s] = G[t][s] 2^(cum_t - cum_{32q}) col_s, unless
@@ -383,7 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // a = dt A has one sign per head, so the block's span is at its ends (uniform)
                     const bool safe = fabsf(m - k.cum_w[min(q * 32 + 31, len - 1)]) <= kSafeSpan;
                     const bool row_ok = t < len;
-                    if (safe) {
+                    if (safe && q < warp - 4 && (warp - 4) * 32 + 31 < len) {
+                        // block strictly below the diagonal for every row of the warp
+                        const float rt = ex2_approx(ct - m);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 cf = *reinterpret_cast<const float2 *>(&k.col_w[q * 32 + 2 * j]);
+                            w[j] = pack_bf16x2(__uint_as_float(gr[2 * j]) * cf.x * rt,
+                                               __uint_as_float(gr[2 * j + 1]) * cf.y * rt);
+                        }
+                    } else if (safe) {
                         const float rt = ex2_approx(ct - m);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
