@@ -258,9 +258,10 @@ uint64_t gbattn_set_wait_timeout_ns(uint64_t ns);
  * off).  Mode 1: in later attn_fwd launches the TMA producer never loads the
  * Q tiles, so the tensor-core warp's wait for them runs out after the wait
  * limit (gbattn_set_wait_timeout_ns); every CTA then stops, frees its tensor
- * memory and exits, and gbattn_check() returns GBATTN_ERR_TIMEOUT.  Nothing
- * faults or traps; the CUDA context stays usable.  Not part of the attention
- * computation (the pages have no counterpart).  Returns the previous mode.
+ * memory and exits, and gbattn_check() returns GBATTN_ERR_TIMEOUT.  Mode 2:
+ * the same for ssd_scan, whose producer then loads no chunk.  Nothing faults
+ * or traps; the CUDA context stays usable.  Not part of the computation (the
+ * pages have no counterpart).  Returns the previous mode.
  */
 int gbattn_set_fault_injection(int mode);
 

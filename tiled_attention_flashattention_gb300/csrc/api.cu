@@ -384,7 +384,7 @@ extern "C" uint64_t gbattn_set_wait_timeout_ns(uint64_t ns)
 
 extern "C" int gbattn_set_fault_injection(int mode)
 {
-    if (mode < 0 || mode > 1) mode = 0;
+    if (mode < 0 || mode > 2) mode = 0;
     return g_inject.exchange(mode);
 }
 

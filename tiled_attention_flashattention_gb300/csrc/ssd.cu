@@ -91,6 +91,7 @@ struct SsdParams {
     float *y;                 // [Bsz][L][H][P]
     float *S_final;           // [Bsz][H][P][N] or nullptr
     int L, H, G, nchunks;
+    int inject;               // 2: the producer loads nothing (tests the bounded waits)
     int *status;
     uint64_t timeout_ns;
 };
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmY);
             bool ok = true;
             int c = 0;
-            for (; c < nch; ++c) {
+            for (; c < nch && p.inject != 2; ++c) {
                 const int u = c & 1;
                 if (c >= 2 && !(ok = mbar_wait(&k.mma_done[u], ((c - 2) >> 1) & 1, ctl))) break;
                 uint8_t *st = smem + u * kStageBytes;
@@ -603,6 +604,7 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
     p.H = H;
     p.G = G;
     p.nchunks = (L + kQ - 1) / kQ;
+    p.inject = env.inject;
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
     static bool configured = false;
