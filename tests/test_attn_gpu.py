@@ -68,6 +68,12 @@ SMALL = [
     (1, 2, 2, 700, 200, 128, False, 50),    # N_q > N_kv: the first rows see no key
     (2, 4, 2, 1030, 1030, 128, False, 300),
     (1, 2, 2, 400, 400, 64, False, 400),    # window >= N: unmasked
+    # rows that visit >= 16 key tiles on average: the two-Q-tile form
+    (1, 2, 2, 300, 2100, 128, False, 0),
+    (1, 2, 2, 300, 2100, 64, False, 0),
+    (2, 2, 1, 257, 3000, 128, True, 0),     # bottom-right causal, ragged query block
+    (1, 2, 2, 2400, 2400, 128, False, 1300),  # symmetric window
+    (1, 1, 1, 640, 4200, 64, True, 0),
 ]
 
 

@@ -30,6 +30,7 @@
 // the exponentials use the stale m_ref (values up to 2^8), which is exact in
 // the end because O and l are divided by the same l built with the same
 // m_ref; it avoids rescaling O (a TMEM round trip) on almost every tile.
+#include <algorithm>
 #include <cmath>
 
 #include "kernels.h"
@@ -40,26 +41,35 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per Q tile
 constexpr int kBN = 128;       // keys per K/V tile
-constexpr int kQTiles = 2;     // Q tiles per CTA
-constexpr int kThreads = 384;
 constexpr int kChunkBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.693147180559945309f;
-// Registers per thread after the per-role split (setmaxnreg): warpgroup 0
-// (producer, MMA issuer, two idle warps) gives registers to the two softmax
-// warpgroups, which hold a 128-float score row per thread.  128 * 104 +
-// 256 * 200 = 64,512, the 384 * 168 registers the block is launched with.
-constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
 
-template <int D>
+// Two forms, by the number kT of 128-row Q tiles per CTA:
+//   kT = 2: one CTA per SM, 384 threads (two softmax warpgroups ping-pong on
+//           the tensor core), 512 TMEM columns, a ring of 5 (d=128) / 10
+//           (d=64) K/V slots;
+//   kT = 1: two CTAs per SM, 256 threads (one softmax warpgroup; the other
+//           CTA fills the tensor core while it works), 256 TMEM columns, a
+//           ring of 2 / 5 slots.  One CTA's start-up and drain overlap the
+//           other's main loop, and the finer work items balance better.
+// Registers per thread after the per-role split (setmaxnreg): warpgroup 0
+// (producer, MMA issuer, idle warps) gives registers to the softmax
+// warpgroups, which hold a 128-float score row per thread.  kT = 2:
+// 128 * 104 + 256 * 200 = 64,512 = 384 * 168; kT = 1: 128 * 64 + 128 * 192
+// (or 56 + 200 where that avoids spills) = 32,768 = 256 * 128, the registers
+// each block is launched with.
+template <int D, int kT>
 struct Cfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kBM * D * 2;
-    static constexpr int kSlots = (D == 128) ? 5 : 10;
-    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kSlots = kT == 2 ? ((D == 128) ? 5 : 10) : ((D == 128) ? 2 : 5);
+    static constexpr uint32_t kTmemCols = kT == 2 ? 512 : 256;
+    static constexpr int kThreads = kT == 2 ? 384 : 256;
+    static constexpr int kMinBlocks = kT == 2 ? 1 : 2;
     // TMEM columns of S_t (P_t overwrites its first 64) and O_t.
     __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-    __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + D * t; }
+    __host__ __device__ static constexpr uint32_t col_o(int t) { return 128u * kT + D * t; }
 };
 
 struct Ctl {
@@ -75,10 +85,10 @@ struct Ctl {
     int sp_lo[2], sp_hi[2];     // block-sparse form: first / last + 1 active key block of each Q tile
 };
 
-template <int D>
+template <int D, int kT>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(kQTiles + Cfg<D>::kSlots) * Cfg<D>::kTileBytes + sizeof(Ctl);
+    return 1024 + static_cast<size_t>(kT + Cfg<D, kT>::kSlots) * Cfg<D, kT>::kTileBytes + sizeof(Ctl);
 }
 
 struct Params {
@@ -89,7 +99,7 @@ struct Params {
     // i' - lo_pad <= j <= i' + hi_pad (and j < N_kv); kNoPad means unbounded.
     int lo_pad, hi_pad;
     int group;          // H / H_kv
-    int n_qblk;         // ceil(N_q / 256)
+    int n_qblk;         // ceil(N_q / (128 kT))
     // Block-sparse form only: a byte per (b, h, 128-row query block, 128-key
     // block), [B][H][ceil(N_q/128)][ceil(N_kv/128)]; 0 skips the block.
     const uint8_t *block_mask;
@@ -114,24 +124,29 @@ __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
     return {static_cast<int>(key_lo / kBN), static_cast<int>((key_hi + kBN - 1) / kBN)};
 }
 
-template <int D, bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kSparse, int kT>
+__global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const Params p)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kT>;
+    constexpr bool kWideSoftmax = kT == 2 || (kSparse && D == 128);
+    constexpr uint32_t kRegsLow = kT == 2 ? 104 : (kWideSoftmax ? 56 : 64);
+    constexpr uint32_t kRegsHigh = kWideSoftmax ? 200 : 192;
+    static_assert(kT == 2 ? 128 * kRegsLow + 256 * kRegsHigh <= 384 * 168
+                          : 128 * kRegsLow + 128 * kRegsHigh == 256 * 128, "register split");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem;                                    // [2][TileBytes]
-    uint8_t *ring = smem + kQTiles * C::kTileBytes;        // [Slots][TileBytes]
+    uint8_t *sQ = smem;                                    // [kT][TileBytes]
+    uint8_t *ring = smem + kT * C::kTileBytes;             // [Slots][TileBytes]
     Ctl &c = *reinterpret_cast<Ctl *>(ring + C::kSlots * C::kTileBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
-    // ---- work item: (batch, head, 256-row query block), longest first
+    // ---- work item: (batch, head, 128 kT-row query block), longest first
     const int nbh = p.B * p.H;
     const int bh = blockIdx.x % nbh;
     const int qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / nbh);
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int lo = 0x7fffffff, hi = -1;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        r0[t] = qb * (kQTiles * kBM) + t * kBM;
+        r0[t] = t < kT ? qb * (kT * kBM) + t * kBM : p.N_q;     // kT = 1: tile 1 is absent
         r1[t] = min(r0[t] + kBM, p.N_q);
         rng[t] = (r0[t] < p.N_q) ? kv_range(r0[t], r1[t], p) : Range{0, 0};
         has[t] = rng[t].lo < rng[t].hi;
@@ -519,14 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, int kT>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
            const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
     static bool configured = false;   // per process; attribute is per function
-    const size_t smem = smem_bytes<D>();
+    const size_t smem = smem_bytes<D, kT>();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse>,
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse, kT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) {
@@ -535,7 +550,7 @@ int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, 
         }
         configured = true;
     }
-    attn_fwd_kernel<D, kSparse><<<grid, kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
+    attn_fwd_kernel<D, kSparse, kT><<<grid, Cfg<D, kT>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
@@ -553,6 +568,27 @@ __global__ void fill_empty_kernel(__nv_bfloat16 *O, float *LSE, size_t rows, int
         LSE[i] = -INFINITY;
     }
 }
+
+// Mean number of 128-key tiles a 128-row query tile visits (the host's copy
+// of kv_range), which decides the form: long rows keep the tensor core busy
+// best with two Q tiles ping-ponging in one CTA; short ones (windows, short
+// causal problems) lose less to CTA start-up and drain with two one-tile
+// CTAs per SM.
+double mean_kv_tiles(int N_q, int N_kv, int lo_pad, int hi_pad)
+{
+    const long long off = static_cast<long long>(N_kv) - N_q;
+    const int n = (N_q + kBM - 1) / kBM;
+    long long total = 0;
+    for (int qt = 0; qt < n; ++qt) {
+        const long long r0 = static_cast<long long>(qt) * kBM, r1 = std::min<long long>(r0 + kBM, N_q);
+        const long long key_lo = std::max(0LL, r0 + off - lo_pad);
+        const long long key_hi = std::min(static_cast<long long>(N_kv), r1 - 1 + off + hi_pad + 1);
+        if (key_hi > key_lo) total += (key_hi + kBN - 1) / kBN - key_lo / kBN;
+    }
+    return n > 0 ? static_cast<double>(total) / n : 0.0;
+}
+
+constexpr double kTwoTileMinKvTiles = 16.0;
 
 }  // namespace
 
@@ -598,7 +634,10 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
     p.block_mask = block_mask;
     p.mask_qb = (N_q + kBM - 1) / kBM;
     p.mask_kb = (N_kv + kBN - 1) / kBN;
-    p.n_qblk = (N_q + kQTiles * kBM - 1) / (kQTiles * kBM);
+    // Q tiles per CTA (see Cfg).  Block-sparse launches use one: their density
+    // is not known here, and sparse rows are short.
+    const int kt = (!block_mask && mean_kv_tiles(N_q, N_kv, p.lo_pad, p.hi_pad) >= kTwoTileMinKvTiles) ? 2 : 1;
+    p.n_qblk = (N_q + kt * kBM - 1) / (kt * kBM);
     p.c = scale * 1.4426950408889634f;
     p.inject = env.inject;
     p.status = env.status;
@@ -608,12 +647,17 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         err = "attn_fwd: problem too large for one launch";
         return 2;
     }
-    if (block_mask) {
-        if (d == 128) return launch<128, true>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
-        return launch<64, true>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    const int g = static_cast<int>(grid);
+    if (kt == 1) {
+        if (block_mask) return d == 128 ? launch<128, true, 1>(tq, tk, tv, to, p, g, env, err)
+                                        : launch<64, true, 1>(tq, tk, tv, to, p, g, env, err);
+        return d == 128 ? launch<128, false, 1>(tq, tk, tv, to, p, g, env, err)
+                        : launch<64, false, 1>(tq, tk, tv, to, p, g, env, err);
     }
-    if (d == 128) return launch<128, false>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
-    return launch<64, false>(tq, tk, tv, to, p, static_cast<int>(grid), env, err);
+    if (block_mask) return d == 128 ? launch<128, true, 2>(tq, tk, tv, to, p, g, env, err)
+                                    : launch<64, true, 2>(tq, tk, tv, to, p, g, env, err);
+    return d == 128 ? launch<128, false, 2>(tq, tk, tv, to, p, g, env, err)
+                    : launch<64, false, 2>(tq, tk, tv, to, p, g, env, err);
 }
 
 }  // namespace gbattn
