@@ -8,7 +8,7 @@
 // base 2 with scale * log2(e) folded into one multiply-add, as in the FlashMLA
 // article's section 3.1 (exp2(acc * scale - max * scale)).
 //
-// How it maps to the GB300 SM (one CTA per SM, 384 threads, 12 warps):
+// How it maps to the GB300 SM, two-Q-tile form (one CTA per SM, 384 threads):
 //   warp 0       TMA producer: two Q tiles (2 x 128 rows) once, then K_j and
 //                V_j tiles into a ring of shared-memory slots (128-byte swizzle);
 //   warp 1       tensor-core issuer: S_t = Q_t K_j^T into TMEM, then
@@ -19,11 +19,13 @@
 // The two Q tiles ping-pong: while the softmax warps work on tile 0's scores,
 // the tensor core computes tile 1's scores and PV products, and vice versa
 // (FlashAttention-2's point about keeping non-matmul work off the critical
-// path, TileLang 学习笔记 "FlashAttention-2 的改进").
+// path, TileLang 学习笔记 "FlashAttention-2 的改进").  The one-Q-tile form
+// (256 threads, warps 0-7) runs two CTAs per SM instead, and the other CTA
+// fills the tensor core while one CTA's softmax works (see Cfg).
 //
-// TMEM (512 columns x 128 lanes of 32 bit): S0 [0,128), S1 [128,256),
-// O0 [256, 256+D), O1 [256+D, 256+2D).  P_t (bf16 pairs) overwrites the first
-// 64 columns of S_t.
+// TMEM (32-bit columns x 128 lanes): S_t at 128 t and O_t after the kT S
+// tiles (two-tile form: S0 [0,128), S1 [128,256), O0 [256, 256+D),
+// O1 [256+D, 256+2D)).  P_t (bf16 pairs) overwrites the first 64 columns of S_t.
 //
 // The running maximum is updated lazily: the reference maximum m_ref moves
 // only when a new score exceeds it by more than 8 in log2 units.  Until then
