@@ -540,17 +540,15 @@ template <int D, bool kSparse, int kT>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
            const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
-    static bool configured = false;   // per process; attribute is per function
+    static std::atomic<uint64_t> configured{0};   // one bit per device
     const size_t smem = smem_bytes<D, kT>();
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse, kT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    {
+        cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(attn_fwd_kernel<D, kSparse, kT>), smem,
+                                            configured);
         if (e != cudaSuccess) {
             err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return 5;
         }
-        configured = true;
     }
     attn_fwd_kernel<D, kSparse, kT><<<grid, Cfg<D, kT>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();

@@ -2,6 +2,7 @@
 // kernel translation units of libgbattn.so.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -17,6 +18,21 @@ enum : int {
     kStatusWaitTimeout = 1,
     kStatusBadLength = 2,     // a per-sequence length outside [0, capacity] (clamped)
 };
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device
+// (the attribute is per device); `done` holds one bit per device ordinal and
+// may be shared by concurrent callers.
+inline cudaError_t set_smem_limit_once(const void *func, size_t bytes, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 struct LaunchEnv {
     cudaStream_t stream;

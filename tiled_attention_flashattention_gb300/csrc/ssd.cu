@@ -607,13 +607,8 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
     p.inject = env.inject;
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
-    static bool configured = false;
-    cudaError_t e = cudaSuccess;
-    if (!configured) {
-        e = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        configured = e == cudaSuccess;
-    }
+    static std::atomic<uint64_t> configured{0};   // one bit per device
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(ssd_scan_kernel), kSmemBytes, configured);
     if (e == cudaSuccess) {
         ssd_scan_kernel<<<dim3(H, Bsz), kThreads, kSmemBytes, env.stream>>>(tc, tb, tx, ty, p);
         e = cudaGetLastError();
