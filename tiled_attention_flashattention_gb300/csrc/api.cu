@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <unordered_map>
+#include <algorithm>
 
 #include "gbattn.h"
 #include "kernels.h"
@@ -97,24 +99,85 @@ EncodeFn tensor_map_encoder()
     });
     return encode;
 }
+
+// Tensor maps are a pure function of their parameters, so encoded maps are
+// cached by value (base address, type, dims, strides, box): repeated calls on
+// the same buffers skip the driver's encode.  Bounded; cleared when full.
+struct MapKey {
+    uintptr_t base;
+    int dtype, rank;
+    uint64_t dims[5], strides[4];
+    uint32_t box[5];
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && dtype == o.dtype && rank == o.rank && std::equal(dims, dims + 5, o.dims) &&
+               std::equal(strides, strides + 4, o.strides) && std::equal(box, box + 5, o.box);
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        uint64_t h = 1469598103934665603ull;
+        auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+        mix(k.base);
+        mix(static_cast<uint64_t>(k.dtype) << 8 | static_cast<uint64_t>(k.rank));
+        for (uint64_t v : k.dims) mix(v);
+        for (uint64_t v : k.strides) mix(v);
+        for (uint32_t v : k.box) mix(v);
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMapCacheMax = 1024;
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// Encode (or fetch) a tiled, 128-byte-swizzled map; rank <= 5.
+CUresult encode_cached(CUtensorMap &desc, CUtensorMapDataType dtype, int rank, const void *base,
+                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box)
+{
+    MapKey key{};
+    key.base = reinterpret_cast<uintptr_t>(base);
+    key.dtype = static_cast<int>(dtype);
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            desc = it->second;
+            return CUDA_SUCCESS;
+        }
+    }
+    EncodeFn encode = tensor_map_encoder();
+    if (!encode) return CUDA_ERROR_NOT_SUPPORTED;
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = encode(&desc, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base), dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        if (g_maps.size() >= kMapCacheMax) g_maps.clear();
+        g_maps.emplace(key, desc);
+    }
+    return r;
+}
 }  // namespace
 
 bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t outer, uint32_t box_rows, std::string &err)
 {
-    EncodeFn encode = tensor_map_encoder();
-    if (!encode) {
+    if (!tensor_map_encoder()) {
         err = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
     }
     const cuuint64_t dims[3] = {cols, rows, outer};
     const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
     const cuuint32_t box[3] = {64, box_rows, 1};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = encode(&desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
     if (r != CUDA_SUCCESS) {
         char buf[160];
         snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu,%llu,%llu] box rows %u",
@@ -129,19 +192,15 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
 bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
                  const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
 {
-    EncodeFn encode = tensor_map_encoder();
-    if (!encode) {
+    if (!tensor_map_encoder()) {
         err = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
     }
     const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
     const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
     const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    CUresult r = encode(&desc, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                        const_cast<void *>(base), d, st, bx, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(desc, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                               base, d, st, bx);
     if (r != CUDA_SUCCESS) {
         char buf[200];
         snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for dims [%llu,%llu,%llu,%llu]",
