@@ -67,6 +67,16 @@ def test_single_key_returns_its_value():
     np.testing.assert_allclose(LSE, dots.numpy(), atol=1e-10, rtol=0)
 
 
+def test_window_one_sees_only_its_own_key():
+    # causal window 1 keeps key j = i only: O_i = V_i and LSE_i = scale q_i . k_i
+    Q, K, V = wl.random_prefill(1, 2, 2, 9, 9, 16, seed=2)
+    scale = 0.29
+    O, LSE = oracle.attn_fwd(Q, K, V, True, 1, scale)
+    np.testing.assert_allclose(O, f64(V).numpy(), atol=TOL, rtol=0)
+    dots = torch.einsum("bhid,bhid->bhi", f64(Q), f64(K)) * scale
+    np.testing.assert_allclose(LSE, dots.numpy(), atol=1e-10, rtol=0)
+
+
 @pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 3), (False, 2)])
 def test_probability_rows_sum_to_one(causal, window):
     Q, K, V = wl.random_prefill(1, 2, 1, 9, 9, 8, seed=2)
