@@ -648,14 +648,12 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         return 2;
     }
     const int g = static_cast<int>(grid);
-    if (kt == 1) {
-        if (block_mask) return d == 128 ? launch<128, true, 1>(tq, tk, tv, to, p, g, env, err)
-                                        : launch<64, true, 1>(tq, tk, tv, to, p, g, env, err);
+    if (block_mask)   // always the one-tile form
+        return d == 128 ? launch<128, true, 1>(tq, tk, tv, to, p, g, env, err)
+                        : launch<64, true, 1>(tq, tk, tv, to, p, g, env, err);
+    if (kt == 1)
         return d == 128 ? launch<128, false, 1>(tq, tk, tv, to, p, g, env, err)
                         : launch<64, false, 1>(tq, tk, tv, to, p, g, env, err);
-    }
-    if (block_mask) return d == 128 ? launch<128, true, 2>(tq, tk, tv, to, p, g, env, err)
-                                    : launch<64, true, 2>(tq, tk, tv, to, p, g, env, err);
     return d == 128 ? launch<128, false, 2>(tq, tk, tv, to, p, g, env, err)
                     : launch<64, false, 2>(tq, tk, tv, to, p, g, env, err);
 }
