@@ -209,6 +209,42 @@ int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_late
                        void *stream);
 
 /*
+ * attn_fwd_host_device_bytes / attn_fwd_host -- attn_fwd with Q, K, V, O and
+ * LSE in HOST memory (same shapes and layouts as attn_fwd; pinned memory
+ * makes the copies asynchronous, pageable memory works but copies
+ * synchronously).  The call copies the inputs to a caller-owned device
+ * buffer, runs attn_fwd and copies O and LSE back, cut into up to 4
+ * contiguous chunks of (batch, KV-head) units so that the host-to-device
+ * copies, the kernels and the device-to-host copies of different chunks
+ * overlap (two library-owned helper streams per device, chained to `stream`
+ * by events).  Asynchronous on `stream`: O and LSE are valid once `stream`
+ * reaches the point of the call (e.g. after gbattn_check(stream)).
+ *   device_buf: at least attn_fwd_host_device_bytes(B, H, H_kv, N_q, N_kv, d)
+ *   bytes, 256-byte aligned, owned by the caller, overwritten.
+ * Errors: as attn_fwd (no alignment rule for the host pointers), plus
+ * GBATTN_ERR_WORKSPACE for a missing or small device buffer.  The size
+ * function returns 0 for an invalid shape.
+ */
+size_t attn_fwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d);
+int attn_fwd_host(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int H_kv, int N_q,
+                  int N_kv, int d, int causal, int window, float scale, void *device_buf, size_t device_bytes,
+                  void *stream);
+
+/*
+ * mla_decode_host_device_bytes / mla_decode_host -- mla_decode with every
+ * tensor in HOST memory (same shapes and layouts), pipelined the same way
+ * over up to 4 chunks of sequences.  device_buf holds the device copies and
+ * the split-KV workspace: at least mla_decode_host_device_bytes(B, H, N_kv,
+ * d_c, d_r) bytes, 256-byte aligned, caller-owned.  Errors: as mla_decode
+ * (no alignment rule for the host pointers), GBATTN_ERR_WORKSPACE for the
+ * device buffer.
+ */
+size_t mla_decode_host_device_bytes(int B, int H, int N_kv, int d_c, int d_r);
+int mla_decode_host(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe, void *O,
+                    float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale, void *device_buf,
+                    size_t device_bytes, void *stream);
+
+/*
  * ssd_scan -- Mamba-2 SSD scan, the chunk-state / chunk-scan linear-attention
  * functions benchmarked in "TileLang: 面向AI系统的可组合分块编程模型" (results,
  * linear attention on H100), with the selective-scan recurrence sketched in

@@ -121,3 +121,32 @@ def test_ssd_scan_argument_errors(lib):
     assert ssd(dt=18) == 3                         # dt not 4-byte aligned
     assert ssd(D=0, fs=0) not in (1, 3)            # D and the final state may be omitted
     assert ssd(Bsz=70000) == 2
+
+
+def test_host_buffer_entry_point_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def attn(B=1, H=2, H_kv=1, N_q=64, N_kv=64, d=128, causal=0, scale=0.1, Q=16, buf=256, nbytes=1 << 30):
+        return lib.attn_fwd_host(vp(Q), vp(16), vp(16), vp(16), vp(16), B, H, H_kv, N_q, N_kv, d, causal, 0,
+                                 ctypes.c_float(scale), vp(buf), nbytes, None)
+    assert attn(B=0) == 1
+    assert attn(H=3, H_kv=2) == 1
+    assert attn(causal=2) == 1
+    assert attn(scale=-1.0) == 1
+    assert attn(d=96) == 2
+    assert attn(Q=0) == 1
+    assert attn(buf=0) == 4                        # no device buffer
+    assert attn(buf=272) == 4                      # not 256-byte aligned
+    assert attn(nbytes=16) == 4                    # too small
+    assert lib.attn_fwd_host_device_bytes(1, 2, 1, 64, 64, 128) == 2 * 32768 + 2 * 16384 + 512
+    assert lib.attn_fwd_host_device_bytes(0, 2, 1, 64, 64, 128) == 0
+
+    def mla(B=2, H=128, N_kv=64, scale=0.04, Qn=16, buf=256, nbytes=1 << 30):
+        return lib.mla_decode_host(vp(Qn), vp(16), vp(16), vp(16), vp(16), vp(16), B, H, N_kv, 512, 64,
+                                   ctypes.c_float(scale), vp(buf), nbytes, None)
+    assert mla(B=0) == 1
+    assert mla(H=64) == 2
+    assert mla(scale=0.0) == 1
+    assert mla(Qn=0) == 1
+    assert mla(buf=0) == 4
+    assert mla(nbytes=16) == 4

@@ -17,7 +17,8 @@ import threading
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_sparse", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_paged",
-           "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan",
+           "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan", "attn_fwd_host",
+           "attn_fwd_host_device_bytes", "mla_decode_host", "mla_decode_host_device_bytes",
            "check", "selftest_umma",
            "set_wait_timeout_ns", "set_fault_injection", "GbattnError", "library_path", "load_library"]
 
@@ -64,6 +65,14 @@ def load_library():
         lib.mla_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, SZ, P]
         lib.mla_decode_paged.restype = I
         lib.ssd_scan.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+        lib.attn_fwd_host_device_bytes.argtypes = [I, I, I, I, I, I]
+        lib.attn_fwd_host_device_bytes.restype = SZ
+        lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_fwd_host.restype = I
+        lib.mla_decode_host_device_bytes.argtypes = [I, I, I, I, I]
+        lib.mla_decode_host_device_bytes.restype = SZ
+        lib.mla_decode_host.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
+        lib.mla_decode_host.restype = I
         lib.ssd_scan.restype = I
         lib.mla_decode_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.mla_decode_noalloc.restype = I
@@ -95,6 +104,19 @@ def _stream_handle(stream) -> int:
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_host(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _need(t: torch.Tensor, name: str, dtype, shape):
@@ -255,6 +277,77 @@ def mla_decode_paged(Q_nope, Q_pe, KV_cache, K_pe_cache, block_table, cache_seql
                               _ptr(cache_seqlens), _ptr(O), _ptr(LSE), B, s_q, H, num_pages, max_pages, page, d_c,
                               d_r, float(scale), _ptr(workspace), workspace.numel(),
                               ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def attn_fwd_host_device_bytes(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int) -> int:
+    return int(load_library().attn_fwd_host_device_bytes(B, H, H_kv, N_q, N_kv, d))
+
+
+def attn_fwd_host(Q, K, V, causal: bool = False, window: int = 0, scale: float | None = None, O=None, LSE=None,
+                  device_buf=None, stream=None):
+    """attn_fwd with host (CPU, ideally pinned) tensors; copies, kernels and copies
+    back are pipelined by the library.  Returns host (O, LSE); they are valid once
+    the stream reaches the call (``check()`` synchronises)."""
+    lib = load_library()
+    B, H, N_q, d = Q.shape
+    H_kv, N_kv = K.shape[1], K.shape[2]
+    _need_host(Q, "Q", torch.bfloat16, None)
+    _need_host(K, "K", torch.bfloat16, (B, H_kv, N_kv, d))
+    _need_host(V, "V", torch.bfloat16, (B, H_kv, N_kv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = Q.is_pinned()
+    if O is None:
+        O = torch.empty((B, H, N_q, d), dtype=torch.bfloat16, pin_memory=pin)
+    if LSE is None:
+        LSE = torch.empty((B, H, N_q), dtype=torch.float32, pin_memory=pin)
+    _need_host(O, "O", torch.bfloat16, (B, H, N_q, d))
+    _need_host(LSE, "LSE", torch.float32, (B, H, N_q))
+    if device_buf is None:
+        device_buf = torch.empty(max(attn_fwd_host_device_bytes(B, H, H_kv, N_q, N_kv, d), 256), dtype=torch.uint8,
+                                 device="cuda")
+    _need(device_buf, "device_buf", torch.uint8, None)
+    rc = lib.attn_fwd_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, H_kv, N_q, N_kv, d,
+                           1 if causal else 0, int(window), float(scale), _ptr(device_buf), device_buf.numel(),
+                           ctypes.c_void_p(_stream_handle(stream)))
+    _raise_if(rc)
+    return O, LSE
+
+
+def mla_decode_host_device_bytes(B: int, H: int = 128, N_kv: int = 4096, d_c: int = 512, d_r: int = 64) -> int:
+    return int(load_library().mla_decode_host_device_bytes(B, H, N_kv, d_c, d_r))
+
+
+def mla_decode_host(Q_nope, Q_pe, KV_latent, K_pe, scale: float | None = None, O=None, LSE=None, device_buf=None,
+                    stream=None):
+    """mla_decode with host (CPU, ideally pinned) tensors, pipelined by the library.
+    Returns host (O, LSE), valid once the stream reaches the call."""
+    lib = load_library()
+    B, H, d_c = Q_nope.shape
+    d_r = Q_pe.shape[-1]
+    N_kv = KV_latent.shape[1]
+    _need_host(Q_nope, "Q_nope", torch.bfloat16, None)
+    _need_host(Q_pe, "Q_pe", torch.bfloat16, (B, H, d_r))
+    _need_host(KV_latent, "KV_latent", torch.bfloat16, (B, N_kv, d_c))
+    _need_host(K_pe, "K_pe", torch.bfloat16, (B, N_kv, d_r))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_c + d_r)
+    pin = Q_nope.is_pinned()
+    if O is None:
+        O = torch.empty((B, H, d_c), dtype=torch.bfloat16, pin_memory=pin)
+    if LSE is None:
+        LSE = torch.empty((B, H), dtype=torch.float32, pin_memory=pin)
+    _need_host(O, "O", torch.bfloat16, (B, H, d_c))
+    _need_host(LSE, "LSE", torch.float32, (B, H))
+    if device_buf is None:
+        device_buf = torch.empty(max(mla_decode_host_device_bytes(B, H, N_kv, d_c, d_r), 256), dtype=torch.uint8,
+                                 device="cuda")
+    _need(device_buf, "device_buf", torch.uint8, None)
+    rc = lib.mla_decode_host(_ptr(Q_nope), _ptr(Q_pe), _ptr(KV_latent), _ptr(K_pe), _ptr(O), _ptr(LSE), B, H, N_kv,
+                             d_c, d_r, float(scale), _ptr(device_buf), device_buf.numel(),
+                             ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return O, LSE
 

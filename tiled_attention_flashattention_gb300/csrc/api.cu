@@ -406,6 +406,240 @@ extern "C" int ssd_scan(const void *x, const float *dt, const float *A, const vo
     return rc;
 }
 
+// ---------------------------------------------------------------------------
+// Host-buffer entry points: the same computation with inputs and outputs in
+// host memory.  The work is cut into a few contiguous chunks of (batch,
+// KV-head) units (each a valid problem on sub-tensors), and per chunk the
+// host-to-device copies (helper stream), the kernels (the caller's stream)
+// and the device-to-host copies (second helper stream) are chained by
+// events, so the copies of one chunk overlap the kernels and copies of the
+// others; the copies in alternate between two streams (two copy engines).  Pinned host memory gives asynchronous copies; pageable memory
+// works but copies synchronously.
+
+namespace {
+constexpr int kPipeChunks = 4;
+
+struct HostPipe {
+    std::mutex mu;            // held while a call enqueues (events are reused)
+    bool init = false;
+    cudaStream_t h2d[2] = {nullptr, nullptr}, d2h = nullptr;   // two copy-in streams: two copy engines
+    cudaEvent_t start = nullptr;
+    cudaEvent_t ev_in[2][kPipeChunks], ev_k[kPipeChunks], ev_out = nullptr;
+};
+HostPipe g_pipe[64];
+
+int host_pipe(HostPipe *&hp)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(GBATTN_ERR_LAUNCH, "host pipeline: no device");
+    hp = &g_pipe[dev];
+    if (hp->init) return GBATTN_OK;
+    const unsigned ef = cudaEventDisableTiming;
+    e = cudaStreamCreateWithFlags(&hp->h2d[0], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->h2d[1], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->start, ef);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_out, ef);
+    for (int i = 0; i < kPipeChunks && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&hp->ev_in[0][i], ef);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_in[1][i], ef);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_k[i], ef);
+    }
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("host pipeline setup: ") + cudaGetErrorString(e));
+    hp->init = true;
+    return GBATTN_OK;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// One host-to-device or device-to-host piece of a chunk.
+struct Piece {
+    void *dst;
+    const void *src;
+    size_t bytes;
+};
+
+// The helper streams start after what the caller queued on `user`.
+cudaError_t pipe_start(HostPipe *hp, cudaStream_t user)
+{
+    cudaError_t e = cudaEventRecord(hp->start, user);
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(hp->h2d[j], hp->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->start, 0);
+    return e;
+}
+
+// Copy a chunk's inputs in, alternating pieces between the two copy-in
+// streams, and make `user` wait for both.
+template <int N>
+cudaError_t pipe_copy_in(HostPipe *hp, int c, const Piece (&in)[N], cudaStream_t user)
+{
+    cudaError_t e = cudaSuccess;
+    int j = 0;
+    for (const Piece &pc : in)
+        if (e == cudaSuccess && pc.bytes) {
+            e = cudaMemcpyAsync(pc.dst, pc.src, pc.bytes, cudaMemcpyHostToDevice, hp->h2d[j]);
+            j ^= 1;
+        }
+    for (int s = 0; s < 2 && e == cudaSuccess; ++s) {
+        e = cudaEventRecord(hp->ev_in[s][c], hp->h2d[s]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(user, hp->ev_in[s][c], 0);
+    }
+    return e;
+}
+}  // namespace
+
+extern "C" size_t attn_fwd_host_device_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d)
+{
+    if (B < 1 || H < 1 || H_kv < 1 || N_q < 0 || N_kv < 0 || d < 1) return 0;
+    const size_t q = static_cast<size_t>(B) * H * N_q * d * 2, kv = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
+    return 2 * round256(q) + 2 * round256(kv) + round256(static_cast<size_t>(B) * H * N_q * 4);
+}
+
+extern "C" int attn_fwd_host(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                             int H_kv, int N_q, int N_kv, int d, int causal, int window, float scale,
+                             void *device_buf, size_t device_bytes, void *stream)
+{
+    g_err.clear();
+    if (B < 1 || H < 1 || H_kv < 1 || N_q < 0 || N_kv < 0)
+        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd_host: need B, H, H_kv >= 1, N_q, N_kv >= 0");
+    if (H % H_kv != 0) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd_host: H must be a multiple of H_kv");
+    if (causal != 0 && causal != 1) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd_host: causal must be 0 or 1");
+    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd_host: scale must be finite and > 0");
+    if (d != 64 && d != 128) return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd_host: d must be 64 or 128");
+    if (static_cast<long long>(B) * H * N_q > (1LL << 40) || static_cast<long long>(N_q) * d > (1LL << 31) ||
+        static_cast<long long>(N_kv) * d > (1LL << 31))
+        return fail(GBATTN_ERR_UNSUPPORTED, "attn_fwd_host: problem too large");
+    if (N_q == 0) return GBATTN_OK;
+    if (!Q || !O || !LSE || (N_kv > 0 && (!K || !V)))
+        return fail(GBATTN_ERR_INVALID_ARG, "attn_fwd_host: null tensor pointer");
+    const size_t need = attn_fwd_host_device_bytes(B, H, H_kv, N_q, N_kv, d);
+    if (!device_buf || device_bytes < need || (reinterpret_cast<uintptr_t>(device_buf) & 255u))
+        return fail(GBATTN_ERR_WORKSPACE, "attn_fwd_host: device buffer missing, smaller than "
+                                          "attn_fwd_host_device_bytes() or not 256-byte aligned");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    HostPipe *hp = nullptr;
+    if ((rc = host_pipe(hp)) != GBATTN_OK) return rc;
+    std::lock_guard<std::mutex> lk(hp->mu);
+
+    const size_t qb = static_cast<size_t>(B) * H * N_q * d * 2, kvb = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
+    uint8_t *dQ = static_cast<uint8_t *>(device_buf), *dK = dQ + round256(qb), *dV = dK + round256(kvb),
+            *dO = dV + round256(kvb), *dL = dO + round256(qb);
+    const int group = H / H_kv, units = B * H_kv;
+    const int nchunk = std::min(kPipeChunks, units);
+    const size_t q_unit = static_cast<size_t>(group) * N_q * d * 2, kv_unit = static_cast<size_t>(N_kv) * d * 2,
+                 l_unit = static_cast<size_t>(group) * N_q * 4;
+    cudaError_t e = pipe_start(hp, env.stream);
+    std::string err;
+    for (int c = 0; c < nchunk && e == cudaSuccess; ++c) {
+        const int u0 = static_cast<int>(static_cast<long long>(c) * units / nchunk);
+        const int u1 = static_cast<int>(static_cast<long long>(c + 1) * units / nchunk);
+        const int nu = u1 - u0;
+        const Piece in[3] = {{dQ + u0 * q_unit, static_cast<const uint8_t *>(Q) + u0 * q_unit, nu * q_unit},
+                             {dK + u0 * kv_unit, K ? static_cast<const uint8_t *>(K) + u0 * kv_unit : nullptr,
+                              nu * kv_unit},
+                             {dV + u0 * kv_unit, V ? static_cast<const uint8_t *>(V) + u0 * kv_unit : nullptr,
+                              nu * kv_unit}};
+        e = pipe_copy_in(hp, c, in, env.stream);
+        if (e != cudaSuccess) break;
+        rc = launch_attn_fwd(dQ + u0 * q_unit, dK + u0 * kv_unit, dV + u0 * kv_unit, dO + u0 * q_unit,
+                             reinterpret_cast<float *>(dL + u0 * l_unit), 1, nu * group, nu, N_q, N_kv, d, causal,
+                             window, scale, nullptr, env, err);
+        if (rc != GBATTN_OK) {
+            g_err = err;
+            return rc;
+        }
+        e = cudaEventRecord(hp->ev_k[c], env.stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->ev_k[c], 0);
+        const Piece out[2] = {{static_cast<uint8_t *>(O) + u0 * q_unit, dO + u0 * q_unit, nu * q_unit},
+                              {reinterpret_cast<uint8_t *>(LSE) + u0 * l_unit, dL + u0 * l_unit, nu * l_unit}};
+        for (const Piece &pc : out)
+            if (e == cudaSuccess) e = cudaMemcpyAsync(pc.dst, pc.src, pc.bytes, cudaMemcpyDeviceToHost, hp->d2h);
+    }
+    // the caller's stream continues once the last copy back is done
+    if (e == cudaSuccess) e = cudaEventRecord(hp->ev_out, hp->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(env.stream, hp->ev_out, 0);
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("attn_fwd_host: ") + cudaGetErrorString(e));
+    return GBATTN_OK;
+}
+
+extern "C" size_t mla_decode_host_device_bytes(int B, int H, int N_kv, int d_c, int d_r)
+{
+    if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0) return 0;
+    const size_t ws = mla_decode_workspace_bytes(B, H, N_kv, d_c);
+    const size_t b = static_cast<size_t>(B);
+    return round256(b * H * d_c * 2) + round256(b * H * d_r * 2) + round256(b * N_kv * d_c * 2) +
+           round256(b * N_kv * d_r * 2) + round256(b * H * d_c * 2) + round256(b * H * 4) + round256(ws);
+}
+
+extern "C" int mla_decode_host(const void *Q_nope, const void *Q_pe, const void *KV_latent, const void *K_pe,
+                               void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
+                               void *device_buf, size_t device_bytes, void *stream)
+{
+    g_err.clear();
+    if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_host: need B, H, N_kv, d_c >= 1 and d_r >= 0");
+    if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_host: scale must be finite and > 0");
+    if (d_c != 512 || d_r != 64 || H != 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_host: supports d_c = 512, d_r = 64, H = 128");
+    if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_host: problem too large");
+    if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)
+        return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_host: null tensor pointer");
+    const size_t need = mla_decode_host_device_bytes(B, H, N_kv, d_c, d_r);
+    if (!device_buf || device_bytes < need || (reinterpret_cast<uintptr_t>(device_buf) & 255u))
+        return fail(GBATTN_ERR_WORKSPACE, "mla_decode_host: device buffer missing, smaller than "
+                                          "mla_decode_host_device_bytes() or not 256-byte aligned");
+    LaunchEnv env;
+    int rc = get_env(env, stream);
+    if (rc != GBATTN_OK) return rc;
+    HostPipe *hp = nullptr;
+    if ((rc = host_pipe(hp)) != GBATTN_OK) return rc;
+    std::lock_guard<std::mutex> lk(hp->mu);
+
+    const size_t qn_u = static_cast<size_t>(H) * d_c * 2, qp_u = static_cast<size_t>(H) * d_r * 2,
+                 kv_u = static_cast<size_t>(N_kv) * d_c * 2, kp_u = static_cast<size_t>(N_kv) * d_r * 2,
+                 o_u = static_cast<size_t>(H) * d_c * 2, l_u = static_cast<size_t>(H) * 4;
+    uint8_t *dQn = static_cast<uint8_t *>(device_buf), *dQp = dQn + round256(B * qn_u),
+            *dKV = dQp + round256(B * qp_u), *dKp = dKV + round256(B * kv_u), *dO = dKp + round256(B * kp_u),
+            *dL = dO + round256(B * o_u), *dW = dL + round256(B * l_u);
+    const size_t ws_bytes = mla_workspace_bytes(B, H, N_kv, d_c, env.num_sms);
+    const int nchunk = std::min(kPipeChunks, B);
+    cudaError_t e = pipe_start(hp, env.stream);
+    std::string err;
+    for (int c = 0; c < nchunk && e == cudaSuccess; ++c) {
+        const int b0 = static_cast<int>(static_cast<long long>(c) * B / nchunk);
+        const int b1 = static_cast<int>(static_cast<long long>(c + 1) * B / nchunk);
+        const size_t nb = static_cast<size_t>(b1 - b0);
+        const Piece in[4] = {{dQn + b0 * qn_u, static_cast<const uint8_t *>(Q_nope) + b0 * qn_u, nb * qn_u},
+                             {dQp + b0 * qp_u, static_cast<const uint8_t *>(Q_pe) + b0 * qp_u, nb * qp_u},
+                             {dKV + b0 * kv_u, static_cast<const uint8_t *>(KV_latent) + b0 * kv_u, nb * kv_u},
+                             {dKp + b0 * kp_u, static_cast<const uint8_t *>(K_pe) + b0 * kp_u, nb * kp_u}};
+        e = pipe_copy_in(hp, c, in, env.stream);
+        if (e != cudaSuccess) break;
+        // chunks run one after another on the caller's stream, so they share the workspace
+        rc = launch_mla_decode(dQn + b0 * qn_u, dQp + b0 * qp_u, dKV + b0 * kv_u, dKp + b0 * kp_u, dO + b0 * o_u,
+                               reinterpret_cast<float *>(dL + b0 * l_u), static_cast<int>(nb), H, N_kv, d_c, d_r,
+                               scale, dW, ws_bytes, env, err);
+        if (rc != GBATTN_OK) {
+            g_err = err;
+            return rc;
+        }
+        e = cudaEventRecord(hp->ev_k[c], env.stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->ev_k[c], 0);
+        const Piece out[2] = {{static_cast<uint8_t *>(O) + b0 * o_u, dO + b0 * o_u, nb * o_u},
+                              {reinterpret_cast<uint8_t *>(LSE) + b0 * l_u, dL + b0 * l_u, nb * l_u}};
+        for (const Piece &pc : out)
+            if (e == cudaSuccess) e = cudaMemcpyAsync(pc.dst, pc.src, pc.bytes, cudaMemcpyDeviceToHost, hp->d2h);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hp->ev_out, hp->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(env.stream, hp->ev_out, 0);
+    if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("mla_decode_host: ") + cudaGetErrorString(e));
+    return GBATTN_OK;
+}
+
 extern "C" int gbattn_check(void *stream)
 {
     g_err.clear();
