@@ -74,6 +74,8 @@ SMALL = [
     (2, 2, 1, 257, 3000, 128, True, 0),     # bottom-right causal, ragged query block
     (1, 2, 2, 2400, 2400, 128, False, 1300),  # symmetric window
     (1, 1, 1, 640, 4200, 64, True, 0),
+    (1, 2, 1, 64, 16384, 128, False, 0),     # few queries, very long keys
+    (1, 2, 2, 100, 9000, 128, True, 0),      # bottom-right causal: every row sees ~8900 keys
 ]
 
 

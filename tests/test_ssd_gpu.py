@@ -68,6 +68,11 @@ CASES = [
     (3, 129, 6, 6, True),     # one group per head, 1-step last chunk
     (2, 256, 4, 1, True),     # two whole chunks
     (1, 700, 4, 4, False),
+    # lengths around the 128-step chunk boundary
+    (1, 127, 2, 1, True),
+    (1, 255, 2, 1, True),
+    (2, 257, 2, 2, True),
+    (1, 384, 3, 1, False),
 ]
 
 
