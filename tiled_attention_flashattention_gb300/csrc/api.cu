@@ -565,10 +565,27 @@ extern "C" int attn_fwd_host(const void *Q, const void *K, const void *V, void *
     return GBATTN_OK;
 }
 
+// Split-KV workspace for the chunks of a host-buffer MLA call: the largest plan
+// over the chunk sizes (the plan depends on the number of sequences).
+static size_t mla_host_chunk_workspace(int B, int H, int N_kv, int d_c, int num_sms)
+{
+    const int n = std::min(kPipeChunks, B);
+    size_t ws = 0;
+    for (int c = 0; c < n; ++c) {
+        const int nb = static_cast<int>(static_cast<long long>(c + 1) * B / n - static_cast<long long>(c) * B / n);
+        ws = std::max(ws, mla_workspace_bytes(nb, H, N_kv, d_c, num_sms));
+    }
+    return ws;
+}
+
 extern "C" size_t mla_decode_host_device_bytes(int B, int H, int N_kv, int d_c, int d_r)
 {
     if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0) return 0;
-    const size_t ws = mla_decode_workspace_bytes(B, H, N_kv, d_c);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    const size_t ws = sms > 0 ? mla_host_chunk_workspace(B, H, N_kv, d_c, sms) : 0;
     const size_t b = static_cast<size_t>(B);
     return round256(b * H * d_c * 2) + round256(b * H * d_r * 2) + round256(b * N_kv * d_c * 2) +
            round256(b * N_kv * d_r * 2) + round256(b * H * d_c * 2) + round256(b * H * 4) + round256(ws);
@@ -605,7 +622,7 @@ extern "C" int mla_decode_host(const void *Q_nope, const void *Q_pe, const void 
     uint8_t *dQn = static_cast<uint8_t *>(device_buf), *dQp = dQn + round256(B * qn_u),
             *dKV = dQp + round256(B * qp_u), *dKp = dKV + round256(B * kv_u), *dO = dKp + round256(B * kp_u),
             *dL = dO + round256(B * o_u), *dW = dL + round256(B * l_u);
-    const size_t ws_bytes = mla_workspace_bytes(B, H, N_kv, d_c, env.num_sms);
+    const size_t ws_bytes = mla_host_chunk_workspace(B, H, N_kv, d_c, env.num_sms);
     const int nchunk = std::min(kPipeChunks, B);
     cudaError_t e = pipe_start(hp, env.stream);
     std::string err;
