@@ -2,10 +2,13 @@
 """Benchmark of the fused attention hot path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-  * prefill attention forward (attn_fwd) on the MHA causal workload
-    B=4, H=16, N_q=N_kv=2048, d=128 (the headline metric, TFLOP/s), and
+  * prefill attention forward (attn_fwd) on the largest single-GPU prefill
+    workload, long-context MHA causal B=1, H=32, N_q=N_kv=16384, d=128 with 1 %
+    of the key rows scaled by 8 (the headline metric, TFLOP/s), and
   * MLA decode (mla_decode) on B=64, H=128, N_kv=4096, d_c=512, d_r=64
     (HBM GB/s, reported in the "decode" object).
+The other prefill workloads (MHA causal B=4 H=16 N=2048, GQA 8k causal, its
+causal and symmetric 256-key windows) are timed kernel-only as extra keys.
 
 Timing: W untimed warm-up steps, then K timed steps.  Inputs are resident in
 HBM; between steps a 256 MiB buffer (> the 129 MB L2) is overwritten so no
@@ -43,7 +46,7 @@ import torch  # noqa: E402
 from tiled_attention_flashattention_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s and MLA-decode HBM GB/s on 1 GB300, % of roofline"
-PREFILL = "mha_causal_b4_h16_n2048_d128"
+PREFILL = "mha_causal_spiky_b1_h32_n16384_d128"
 DECODE = "mla_decode_b64_h128_nkv4096"
 FLUSH_BYTES = 256 << 20
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -68,6 +71,27 @@ def allowed_pairs(N_q: int, N_kv: int, causal: bool, window: int) -> int:
     """Number of (query, key) pairs the mask keeps, per (batch, head)."""
     lo, hi = key_bounds(np.arange(N_q, dtype=np.int64), N_q, N_kv, causal, window)
     return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def prefill_form(c: wl.PrefillCase) -> str:
+    """Which instance of the prefill kernel the library launches for this
+    workload: the host picks two 128-row Q tiles per CTA when a query tile
+    visits at least 16 key tiles on average, else one (same rule as the
+    launcher)."""
+    lo, hi = key_bounds(np.arange(c.N_q, dtype=np.int64), c.N_q, c.N_kv, c.causal, c.window)
+    tiles = []
+    for t0 in range(0, c.N_q, 128):
+        klo, khi = lo[t0:t0 + 128].min(), hi[t0:t0 + 128].max() + 1
+        tiles.append(max(0, -(-khi // 128) - klo // 128) if khi > klo else 0)
+    kt = 2 if np.mean(tiles) >= 16 else 1
+    return f"attn_fwd_kernel<{c.d}, dense, {kt} Q tile{'s' if kt == 2 else ''} per CTA>"
+
+
+def bench_config(pc, dc, world):
+    return {"workload": pc.name, "B": pc.B, "H": pc.H, "H_kv": pc.H_kv, "N_q": pc.N_q, "N_kv": pc.N_kv,
+            "d": pc.d, "causal": pc.causal, "window": pc.window, "decode_workload": dc.name,
+            "parallelism": f"independent shards x{world}" if world > 1 else "single GPU",
+            "l2": "256 MiB buffer overwritten between steps (outside the timed kernels)"}
 
 
 def prefill_flops(c: wl.PrefillCase) -> float:
@@ -122,16 +146,22 @@ def traffic_per_launch(kernel_key: str, source: str, workload: str):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi polled every 20 ms in a child process (read-only queries).
+    start() returns once the first sample has been written, so that a short
+    timed region that follows is covered; summary(t0, t1) reports the samples
+    from wall time t0 to t1 (time.time())."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
+        self.rows = []
         self.path = os.path.join(tempfile.gettempdir(), f"gbattn_clocks_{os.getpid()}.csv")
 
-    def start(self):
+    def start(self, wait_s: float = 5.0):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
@@ -140,31 +170,56 @@ class ClockSampler:
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t_end = time.time() + wait_s
+        while time.time() < t_end:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+
+    @staticmethod
+    def _parse_time(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                continue
+        return None
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                self.rows.append((self._parse_time(parts[0]), float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
+
+    def summary(self, t0: float, t1: float, timed=None):
+        """Samples taken from t0 to t1 (wall clock; nvidia-smi stamps local time).
+        timed = (ta, tb): also count the samples inside the timed region."""
+        rows = [r for r in self.rows if r[0] is not None and t0 - 0.05 <= r[0] <= t1 + 0.05]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for _, _, flags in rows for k, v in enumerate(flags) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({self.NAMES[k] for r in rows for k, v in enumerate(r[3]) if v == "Active"})
+        out = {"sm_mhz": statistics.median(r[1] for r in rows), "sm_mhz_min": min(r[1] for r in rows),
+               "sm_max_mhz": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows),
+               "window": "from the first timed step to the end of the extra workloads"}
+        if timed:
+            ta, tb = timed
+            out["samples_in_timed_steps"] = sum(1 for r in rows if ta - 0.025 <= r[0] <= tb + 0.025)
+        return out
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -263,8 +318,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": pc.name, "B": pc.B, "H": pc.H, "H_kv": pc.H_kv, "N_q": pc.N_q,
-                       "N_kv": pc.N_kv, "d": pc.d, "causal": pc.causal, "window": pc.window},
+            "config": bench_config(pc, wl.WORKLOADS[args.decode_workload], world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.default_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -441,6 +495,35 @@ def other_prefill_workloads(gb, dev, skip, peaks, flush, reps=10):
     return out
 
 
+def peaks_now():
+    return load_peaks()[0]
+
+
+def copy_ceiling(dev, ins, outs, flush, reps=5):
+    """Seconds per step to move the given pinned host tensors to the device and
+    the given device-sized results back with plain cudaMemcpyAsync (inputs on
+    one stream, results on another, as in the host-buffer entry points), median
+    of reps, wall time bracketed by device synchronisation."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    d_in = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in ins]
+    d_out = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in outs]
+    ts = []
+    for _ in range(reps + 1):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in, ins):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for h, d in zip(outs, d_out):
+                h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+        ts.append(time.perf_counter() - t0)
+    del d_in, d_out
+    return statistics.median(ts[1:])
+
+
 def run_ours(args, rank, world, local):
     import tiled_attention_flashattention_gb300 as gb
     if not torch.cuda.is_available():
@@ -481,22 +564,23 @@ def run_ours(args, rank, world, local):
         if events:
             events[2].record(stream)
 
+    sampler = ClockSampler(local)
+    sampler.start()          # returns once nvidia-smi has written its first sample
     for _ in range(max(3, args.warmup)):
         step()
     gb.check()
     n_ev = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
-    sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
-    sampler.start()
+    t_wall0 = time.time()
     t0 = time.perf_counter()
     for k in range(args.steps):
         step(evs[k])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    t_wall1 = time.time()
     barrier(world)
-    clocks = sampler.stop()
     gb.check()
     t_pre = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3   # seconds
     t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
@@ -546,6 +630,20 @@ def run_ours(args, rank, world, local):
     d2h_p = O.numel() * 2 + LSE.numel() * 4
     h2d_d = sum(x.numel() * x.element_size() for x in dec_h)
     d2h_d = Od.numel() * 2 + Ld.numel() * 4
+    # the same bytes through plain pinned copies (no kernel): what the copies alone allow
+    ceil_p = copy_ceiling(dev, [Qh_p, Kh_p, Vh_p], [O_h, L_h], flush)
+    ceil_d = copy_ceiling(dev, dec_p, [Od_h, Ld_h], flush)
+
+    extra = {}
+    if not args.no_extra:
+        extra["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks_now(), flush)
+        extra["decode_paged"] = paged_decode_workload(gb, dev, peaks_now(), flush)
+        extra["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks_now(), flush)
+        extra["ssd_scan"] = ssd_workload(gb, dev, peaks_now(), flush)
+    torch.cuda.synchronize()
+    t_wall2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall2, timed=(t_wall0, t_wall1))
 
     if rank != 0:
         return
@@ -554,7 +652,7 @@ def run_ours(args, rank, world, local):
     roof_p = {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
               "frac": tflops / world / peaks["bf16_tflops"],
               "traffic": traffic_per_launch("attn_fwd_kernel", "attn_fwd.cu", pc.name),
-              "kernel": "attn_fwd_kernel<128>", "peak_source": f"{peak_src} bf16 dense (burst)",
+              "kernel": prefill_form(pc), "peak_source": f"{peak_src} bf16 dense (burst)",
               "algorithmic_flops_per_launch": fl_p}
     roof_d = {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
               "frac": gbs / world / peaks["hbm_gbs"],
@@ -566,10 +664,7 @@ def run_ours(args, rank, world, local):
         "warmup": max(3, args.warmup), "ms_per_step": (t_pre + t_dec) / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": pc.name, "B": pc.B, "H": pc.H, "H_kv": pc.H_kv, "N_q": pc.N_q, "N_kv": pc.N_kv,
-                   "d": pc.d, "causal": pc.causal, "window": pc.window, "decode_workload": dc.name,
-                   "parallelism": f"independent shards x{world}" if world > 1 else "single GPU",
-                   "l2": "256 MiB buffer overwritten between steps (outside the timed kernels)"},
+        "config": bench_config(pc, dc, world),
         "roofline": roof_p,
         "decode": {"metric": "MLA-decode HBM GB/s", "value": gbs, "unit": "GB/s",
                    "ms_per_launch": dec_launch_s * 1e3, "roofline": roof_d,
@@ -578,16 +673,21 @@ def run_ours(args, rank, world, local):
                            "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": d2h_d}},
         "e2e": {"value": fl_p * e2e_steps * world / e2e_pre / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": d2h_p},
+        "e2e_ceiling": {
+            "what": "the e2e bytes of one step moved by plain pinned cudaMemcpyAsync (inputs in and results "
+                    "out on two streams, no kernel), and the metric that copy time alone would allow",
+            "prefill": {"copy_ms": ceil_p * 1e3, "gbs": (h2d_p + d2h_p) / ceil_p / 1e9,
+                        "value": fl_p * world / ceil_p / 1e12, "unit": "TFLOP/s",
+                        "e2e_frac": (fl_p * e2e_steps / e2e_pre) / (fl_p / ceil_p)},
+            "decode": {"copy_ms": ceil_d * 1e3, "gbs": (h2d_d + d2h_d) / ceil_d / 1e9,
+                       "value": by_d * world / ceil_d / 1e9, "unit": "GB/s",
+                       "e2e_frac": (by_d * e2e_steps / e2e_dec) / (by_d / ceil_d)}},
         "gpu_launches": args.steps * (1 + n_dec_launches),
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "kernel_source": {"attn_fwd": src_p, "mla_decode": src_d},
     }
-    if not args.no_extra:
-        line["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks, flush)
-        line["decode_paged"] = paged_decode_workload(gb, dev, peaks, flush)
-        line["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks, flush)
-        line["ssd_scan"] = ssd_workload(gb, dev, peaks, flush)
+    line.update(extra)
     if world == 1 and not args.no_cpu_baseline:
         pcase = {"case": pc, "inputs": (Qh, Kh, Vh)}
         line["cpu_baseline"] = cpu_baseline(pcase, None, budget_s=args.cpu_budget)

@@ -871,12 +871,20 @@ struct Plan {
     size_t slots;
 };
 
-// Cluster count: as many 2-CTA clusters as are co-resident on the device
-// (queried once per process), never more than the number of key tiles.
+// Cluster count: as many 2-CTA clusters as are co-resident on the current
+// device, queried once per device (the value depends on the device's SM count
+// and shared memory), under a lock so that concurrent first calls agree.
 int resident_clusters(int num_sms)
 {
-    static int cached = -1;
-    if (cached > 0) return cached;
+    static std::mutex mu;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return num_sms / 2;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] > 0) return cached[dev];
     int n = 0;
     if (cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) == cudaSuccess) {
@@ -895,7 +903,7 @@ int resident_clusters(int num_sms)
     }
     cudaGetLastError();
     if (n <= 0) n = num_sms / 2;
-    cached = n;
+    cached[dev] = n;
     return n;
 }
 

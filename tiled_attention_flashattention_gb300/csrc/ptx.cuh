@@ -177,19 +177,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in
-// cta_mask (this cluster), completing bytes on the mbarrier at the same
-// offset in each of them.
-__device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
-                                                      int y, int z, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
-        : "memory");
-}
-
 // Tiled 3-D store shared -> global (bulk-group completion).  Elements of the
 // box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
@@ -350,17 +337,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
-        : "memory");
-}
-
-// As umma_commit, arriving on the mbarrier at the same offset in every CTA of
-// cta_mask (this cluster).
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 
