@@ -189,6 +189,31 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
     return true;
 }
 
+bool make_tma_bf16_chunked(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows, uint64_t outer,
+                           uint32_t box_rows, uint32_t box_chunks, std::string &err)
+{
+    if (!tensor_map_encoder()) {
+        err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    // [outer][rows][cols] viewed as (64 columns, rows, cols / 64 chunks, outer):
+    // the chunk index is outside the row index in the box, so a box lands in
+    // shared memory as [chunk][row][64 columns].
+    const cuuint64_t dims[4] = {64, rows, cols / 64, outer};
+    const cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
+    const cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
+    CUresult r = encode_cached(desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box);
+    if (r != CUDA_SUCCESS) {
+        char buf[200];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for chunked [%llu,%llu,%llu] box %u rows x %u chunks",
+                 static_cast<int>(r), static_cast<unsigned long long>(outer), static_cast<unsigned long long>(rows),
+                 static_cast<unsigned long long>(cols), box_rows, box_chunks);
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
 bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
                  const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
 {

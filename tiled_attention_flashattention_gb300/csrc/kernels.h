@@ -84,6 +84,14 @@ int launch_selftest_umma(const void *A, const void *B, const void *P, const void
 // Returns false and fills err on failure.
 bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t outer, uint32_t box_rows, std::string &err);
+// The same row-major bf16 tensor [outer][rows][cols] (cols % 64 == 0) viewed
+// as 4-D (64 columns, rows, cols / 64, outer) with a box of 64 columns x
+// box_rows rows x box_chunks 64-column chunks: one load brings box_chunks
+// 128-byte-swizzled [box_rows][64] blocks, stored one after another in
+// shared memory ([chunk][row][64]), i.e. several 64-column boxes in one TMA
+// request.
+bool make_tma_bf16_chunked(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows, uint64_t outer,
+                           uint32_t box_rows, uint32_t box_chunks, std::string &err);
 // 4-D bf16 (f32 = false) or fp32 tensor map, 128-byte swizzle; dims innermost
 // first, strides in bytes of dims 1..3, box in elements (inner box 128 bytes).
 bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],

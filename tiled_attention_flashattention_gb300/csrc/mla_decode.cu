@@ -97,6 +97,7 @@ struct Ctl {
 constexpr size_t kSmemBytes =
     1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * static_cast<size_t>(kXBytes) + sizeof(Ctl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kStages % 2 == 0, "the two producer warps own alternate stages");
 
 struct Params {
     __nv_bfloat16 *O;
@@ -261,17 +262,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int b_first = t_end > t_begin ? S.of_tile(t_begin) : 0;
     const int b_last = t_end > t_begin ? S.of_tile(t_end - 1) : -1;
 
-    if (warp == 0) {
-        // =================== TMA producer ===================
+    if (warp == 0 || warp == 2) {
+        // =================== TMA producers ===================
+        // Two producer warps own alternate ring stages (kStages is even, so a
+        // stage always belongs to the same warp): a thread's bulk-tensor loads
+        // are served one after another, and two issuing warps double the
+        // request rate.  Both walk the same slot sequence and issue their own.
+        const int mine = warp == 0 ? 0 : 1;
         if (lane == 0) {
-            tma_prefetch_desc(&tmKV);
-            tma_prefetch_desc(&tmKp);
-            tma_prefetch_desc(&tmQn);
-            tma_prefetch_desc(&tmQp);
+            if (mine == 0) {
+                tma_prefetch_desc(&tmKV);
+                tma_prefetch_desc(&tmKp);
+                tma_prefetch_desc(&tmQn);
+                tma_prefetch_desc(&tmQp);
+            }
             bool ok = true;
             int it = 0;
             const uint32_t kvbytes = nch * kKvChunk;
             const uint32_t qbytes = rank == 0 ? 2 * kQChunk : 2 * kQChunk + kQChunk / 2;
+            const int chunk0 = static_cast<int>(rank) * (kHalf / 64);     // this CTA's first latent chunk
             for (int b = b_first; b <= b_last && ok; ++b) {
                 const long long P0 = S.start(b);
                 const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
@@ -281,25 +290,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // paged: the page of the next tile, loaded one tile ahead of its use
                 int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : b;
                 // This sequence's query part: two ring slots, each [128 heads x 64 dims]
-                // chunks 2i and 2i + 1 of Q_nope, plus heads [64i, 64i + 64) of Q_pe on CTA 1.
-                for (int qi = 0; qi < 2; ++qi) {
+                // chunks 2i and 2i + 1 of Q_nope (one request), plus heads [64i, 64i + 64)
+                // of Q_pe on CTA 1.
+                for (int qi = 0; qi < 2; ++qi, ++it) {
+                    if ((it & 1) != mine) continue;
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], qbytes);
-                    tma_load_3d(dst, &tmQn, &c.full[s], dim0 + 2 * qi * 64, 0, b);
-                    tma_load_3d(dst + kQChunk, &tmQn, &c.full[s], dim0 + (2 * qi + 1) * 64, 0, b);
+                    tma_load_4d(dst, &tmQn, &c.full[s], 0, 0, chunk0 + 2 * qi, b);
                     if (rank == 1) tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], 0, qi * 64, b);
-                    ++it;
                 }
-                for (long long x = x0; x < x1 && ok; ++x) {
-                    if (x == max(x0, x1 - 4) && b < b_last) {
+                for (long long x = x0; x < x1 && ok; ++x, ++it) {
+                    if (mine == 0 && x == max(x0, x1 - 4) && b < b_last) {
                         // The next range's query and first key tiles into L2 a few tiles
                         // ahead: its two query slots take half the ring, so its first
                         // tile is loaded late and must not also pay the HBM latency.
                         const int nb = S.of_tile(x1);          // the next sequence with tiles here
-                        for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmQn, dim0 + ch * 64, 0, nb);
+                        tma_prefetch_l2_4d(&tmQn, 0, 0, chunk0, nb);
                         if (rank == 1) {
                             tma_prefetch_l2_3d(&tmQp, 0, 0, nb);
                             tma_prefetch_l2_3d(&tmQp, 0, 64, nb);
@@ -309,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const int r = kPaged ? 0 : j * kBN;
                             const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(nb / p.q_per_seq) * p.max_pages + j)
                                                  : nb;
-                            for (int ch = 0; ch < 4; ++ch) tma_prefetch_l2_3d(&tmKV, dim0 + ch * 64, r, o);
+                            tma_prefetch_l2_4d(&tmKV, 0, r, chunk0, o);
                             if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, r, o);
                         }
                     }
@@ -319,22 +328,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int row0 = kPaged ? 0 : tile * kBN;
                     const int outer = outer_next;
                     if (kPaged && x + 1 < x1) outer_next = __ldg(pages + tile + 1);
+                    if ((it & 1) != mine) continue;
                     const int s = it % kStages;
                     const uint32_t round = static_cast<uint32_t>(it / kStages);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], kvbytes);
-                    for (int ch = 0; ch < 4; ++ch)
-                        tma_load_3d(dst + ch * kKvChunk, &tmKV, &c.full[s], dim0 + ch * 64, row0, outer);
+                    tma_load_4d(dst, &tmKV, &c.full[s], 0, row0, chunk0, outer);   // 4 latent chunks
                     if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, row0, outer);
-                    ++it;
                 }
+                if (!ok) break;
             }
             if (!ok) {
+                // Let every load this warp issued land before the CTA exits.
                 volatile int no_abort = 0;
                 const WaitCtl drain{&no_abort, p.status, p.timeout_ns};
                 for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
-                    mbar_wait(&c.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, drain);
+                    if ((i & 1) == mine)
+                        mbar_wait(&c.full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u, drain);
             }
         }
     } else if (warp == 1) {
@@ -1004,8 +1015,10 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
         return 4;
     }
     CUtensorMap tkv, tkp, tqn, tqp;
-    if (!make_tma_bf16_3d(tkv, KV_latent, d_c, N_kv, B, kBN, err) || !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
-        !make_tma_bf16_3d(tqn, Q_nope, d_c, kH, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
+    if (!make_tma_bf16_chunked(tkv, KV_latent, d_c, N_kv, B, kBN, 4, err) ||
+        !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
+        !make_tma_bf16_chunked(tqn, Q_nope, d_c, kH, B, kH, 2, err) ||
+        !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
         return 5;
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
@@ -1083,9 +1096,10 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
         return 4;
     }
     CUtensorMap tkv, tkp, tqn, tqp;
-    if (!make_tma_bf16_3d(tkv, KV_cache, d_c, kBN, num_pages, kBN, err) ||
+    if (!make_tma_bf16_chunked(tkv, KV_cache, d_c, kBN, num_pages, kBN, 4, err) ||
         !make_tma_bf16_3d(tkp, K_pe_cache, d_r, kBN, num_pages, kBN, err) ||
-        !make_tma_bf16_3d(tqn, Q_nope, d_c, kH, B, kH, err) || !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
+        !make_tma_bf16_chunked(tqn, Q_nope, d_c, kH, B, kH, 2, err) ||
+        !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
         return 5;
     const size_t slots = static_cast<size_t>(C) * 2;
     Params p;
