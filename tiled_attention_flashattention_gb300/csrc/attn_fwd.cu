@@ -438,16 +438,23 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                     if (!allowed) s[i] = -INFINITY;
                 }
             }
-            float mx = s[0];
+            // Row maximum as four independent chains and a tree, not one
+            // 127-deep dependency chain.
+            float m4[4];
 #pragma unroll
-            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+            for (int q = 0; q < 4; ++q) {
+                m4[q] = s[q];
+#pragma unroll
+                for (int i = 4 + q; i < 128; i += 4) m4[q] = fmaxf(m4[q], s[i]);
+            }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 
             const bool move = mx > m_ref + thr;
             const float new_ref = move ? mx : m_ref;
             const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
             m_ref = new_ref;
             const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-            float sum = 0.f;
+            float sum2[2] = {0.f, 0.f};                 // independent partial sums
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t pk[16];
@@ -455,12 +462,12 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                 for (int i = 0; i < 16; ++i) {
                     const float p0 = ex2_approx(fmaf(s[q * 32 + 2 * i], cexp, -base));
                     const float p1 = ex2_approx(fmaf(s[q * 32 + 2 * i + 1], cexp, -base));
-                    sum += p0 + p1;
+                    sum2[i & 1] += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_x16(tS + q * 16, pk);
             }
-            l = l * alpha + sum;
+            l = l * alpha + (sum2[0] + sum2[1]);
             if (n > 0 && __any_sync(0xffffffffu, move)) {
                 // O_t already holds the PV products of earlier tiles (their
                 // completion is covered by this tile's S commit); rescale it

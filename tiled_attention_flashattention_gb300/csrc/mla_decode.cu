@@ -636,24 +636,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < kBU; ++k)
                             if (key0 + k >= n_keys) s[k] = -INFINITY;
                     }
-                    float mx = s[0];
+                    float m4[4];
 #pragma unroll
-                    for (int k = 1; k < kBU; ++k) mx = fmaxf(mx, s[k]);
+                    for (int q = 0; q < 4; ++q) {
+                        m4[q] = s[q];
+#pragma unroll
+                        for (int k = 4 + q; k < kBU; k += 4) m4[q] = fmaxf(m4[q], s[k]);
+                    }
+                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                     const bool move = mx > m_ref + thr;
                     const float new_ref = move ? mx : m_ref;
                     const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
                     m_ref = new_ref;
                     const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-                    float sum = 0.f;
+                    float sum2[2] = {0.f, 0.f};
                     uint32_t pk[kBU / 2];
 #pragma unroll
                     for (int k = 0; k < kBU / 2; ++k) {
                         const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
                         const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
-                        sum += p0 + p1;
+                        sum2[k & 1] += p0 + p1;
                         pk[k] = pack_bf16x2(p0, p1);
                     }
-                    l = l * alpha + sum;
+                    l = l * alpha + (sum2[0] + sum2[1]);
                     // P buffer h was read by the MMA of unit (t - 1, h).
                     if (t > 0) okw = __all_sync(0xffffffffu, mbar_wait(&c.pfree[h], (t - 1) & 1u, ctl)) && okw;
                     // O must hold every earlier unit of this range before it is rescaled.
