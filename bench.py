@@ -325,19 +325,29 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def paged_decode_workload(gb, dev, peaks, flush, reps=10):
-    """Kernel-only HBM GB/s of mla_decode_paged on 64 sequences with seeded
-    lengths in [2048, 6144] keys (mean about 4096) in 64-key pages placed at
-    random (inputs resident, L2 flushed before each timed call).  Algorithmic
-    bytes: every key row read once (576 bf16), Q read once, O and LSE written
-    once."""
+def paged_inputs(dev, H=128, s_q=1):
+    """64 sequences with seeded lengths in [2048, 6144] keys (mean about 4096),
+    64-key pages placed at random, H heads and s_q query tokens per sequence."""
     g = torch.Generator().manual_seed(wl.SEED_BASE + 5)
     lens = torch.randint(2048, 6145, (64,), generator=g).tolist()
-    Qn, Qp, KV, Kp, table, L = (x.to(dev) for x in wl.random_mla_paged(128, lens, seed=wl.SEED_BASE + 5))
-    B, H = len(lens), 128
-    O = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
-    LSE = torch.empty(B, H, dtype=torch.float32, device=dev)
-    ws = torch.empty(gb.mla_decode_paged_workspace_bytes(B, 1), dtype=torch.uint8, device=dev)
+    xs = [x.to(dev) for x in wl.random_mla_paged(H, lens, seed=wl.SEED_BASE + 5, s_q=s_q)]
+    return lens, xs
+
+
+def paged_decode_workload(gb, dev, peaks, flush, reps=10, H=128, s_q=1):
+    """Kernel-only HBM GB/s of mla_decode_paged on 64 sequences with seeded
+    lengths in [2048, 6144] keys (mean about 4096) in 64-key pages placed at
+    random (inputs resident, L2 flushed before each timed call).  With H heads
+    and s_q query tokens per sequence; when s_q * H <= 128 all of a sequence's
+    tokens share one 128-row tile and its keys are read once.  Algorithmic
+    bytes: every key row read once (576 bf16), Q read once, O and LSE written
+    once."""
+    lens, (Qn, Qp, KV, Kp, table, L) = paged_inputs(dev, H, s_q)
+    B = len(lens)
+    lead = (B, s_q, H) if s_q > 1 else (B, H)
+    O = torch.empty(*lead, 512, dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty(*lead, dtype=torch.float32, device=dev)
+    ws = torch.empty(gb.mla_decode_paged_workspace_bytes(B, s_q, H), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(576)
     call = lambda: gb.mla_decode_paged(Qn, Qp, KV, Kp, table, L, scale=scale, O=O, LSE=LSE, workspace=ws)
     for _ in range(3):
@@ -354,10 +364,13 @@ def paged_decode_workload(gb, dev, peaks, flush, reps=10):
         total += e0.elapsed_time(e1) / 1e3
     gb.check()
     t = total / reps
-    by = float(sum(lens) * 576 * 2 + B * H * 576 * 2 + B * H * 512 * 2 + B * H * 4)
+    rows = B * s_q * H
+    by = float(sum(lens) * 576 * 2 + rows * 576 * 2 + rows * 512 * 2 + rows * 4)
     gbs = by / t / 1e9
-    return {"workload": "mla_paged_b64_h128_len2048to6144_page64", "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
-            "ms": t * 1e3, "total_keys": int(sum(lens)), "algorithmic_bytes": by}
+    name = "mla_paged_b64_h128_len2048to6144_page64" if (H, s_q) == (128, 1) else \
+        f"mla_paged_b64_h{H}_sq{s_q}_len2048to6144_page64"
+    return {"workload": name, "gbs": gbs, "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "ms": t * 1e3, "total_keys": int(sum(lens)), "algorithmic_bytes": by, "heads": H, "s_q": s_q}
 
 
 def sparse_pairs(mask, N_q: int, N_kv: int, causal: bool, window: int, block: int = 128) -> int:
@@ -638,6 +651,7 @@ def run_ours(args, rank, world, local):
     if not args.no_extra:
         extra["prefill_workloads"] = other_prefill_workloads(gb, dev, pc.name, peaks_now(), flush)
         extra["decode_paged"] = paged_decode_workload(gb, dev, peaks_now(), flush)
+        extra["decode_paged_packed"] = paged_decode_workload(gb, dev, peaks_now(), flush, H=64, s_q=2)
         extra["prefill_sparse"] = sparse_prefill_workload(gb, dev, peaks_now(), flush)
         extra["ssd_scan"] = ssd_workload(gb, dev, peaks_now(), flush)
     torch.cuda.synchronize()
@@ -709,6 +723,11 @@ def run_profile_case(args, local):
         LSE = torch.empty(pc.B, pc.H, pc.N_q, dtype=torch.float32, device=dev)
         for _ in range(args.warmup + args.steps):
             gb.attn_fwd(Q, K, V, causal=pc.causal, window=pc.window, scale=pc.softmax_scale(), O=O, LSE=LSE)
+    elif args.profile == "paged-packed":
+        lens, (Qn, Qp, KV, Kp, table, L) = paged_inputs(dev, H=64, s_q=2)
+        ws = torch.empty(gb.mla_decode_paged_workspace_bytes(len(lens), 2, 64), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup + args.steps):
+            gb.mla_decode_paged(Qn, Qp, KV, Kp, table, L, workspace=ws)
     elif args.profile == "ssd":
         c = wl.SsdCase(**{**wl.SSD_WORKLOAD.__dict__, "Bsz": args.ssd_batch or wl.SSD_WORKLOAD.Bsz})
         x, dt, A, B, C, D = (t.to(dev) for t in wl.ssd_inputs(c))
@@ -742,7 +761,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other prefill workloads")
-    ap.add_argument("--profile", choices=["prefill", "decode", "ssd"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "paged-packed", "ssd"], default=None,
                     help="only launch the selected kernel warmup+steps times (for ncu captures)")
     ap.add_argument("--ssd-batch", type=int, default=0,
                     help="with --profile ssd: batch entries of the SSD workload (default: all)")

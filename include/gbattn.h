@@ -122,7 +122,9 @@ size_t mla_decode_workspace_bytes(int B, int H, int N_kv, int d_c);
  *   Q_nope bf16 [B, H, d_c]   Q_pe bf16 [B, H, d_r]
  *   KV_latent bf16 [B, N_kv, d_c]   K_pe bf16 [B, N_kv, d_r]
  *   O bf16 [B, H, d_c] (written)    LSE fp32 [B, H] (written)
- *   d_c = 512, d_r = 64, H = 128 (one 128-row tile of heads), B >= 1,
+ *   d_c = 512, d_r = 64, 1 <= H <= 128 (the heads are the rows of one
+ *   128-row tile, section 2.1's [block_H, dim] query tile; with H < 128 the
+ *   other rows are padding that is neither read from Q nor written), B >= 1,
  *   N_kv >= 1 (same for every sequence), scale finite and > 0.
  *   workspace: device buffer of at least mla_decode_workspace_bytes(B, H,
  *   N_kv, d_c) bytes, 16-byte aligned, owned by the caller; it holds the
@@ -152,8 +154,11 @@ size_t mla_decode_paged_workspace_bytes(int B, int s_q, int H, int d_c);
  * tokens per sequence (several new tokens at once), the tokens are the last
  * s_q positions of the sequence and attend causally: token t sees keys
  * j < cache_seqlens[b] - (s_q - 1 - t).  A row without keys gets O = 0 and
- * LSE = -inf.  Each query token reads the sequence's keys once (the key
- * tiles are not shared between the tokens of a sequence).
+ * LSE = -inf.  The query rows of a sequence ([s_q][H], token-major) are cut
+ * into 128-row tiles of whole tokens (max(1, 128 / H) tokens each): when
+ * s_q * H <= 128 all of a sequence's tokens share one tile and its keys are
+ * read from memory once, each row masked to its own token's keys; with
+ * H = 128 every token is its own tile and reads the keys again.
  *
  * Arguments
  *   Q_nope bf16 [B, s_q, H, d_c]   Q_pe bf16 [B, s_q, H, d_r]
@@ -162,7 +167,7 @@ size_t mla_decode_paged_workspace_bytes(int B, int s_q, int H, int d_c);
  *     sequence's last page are not read)
  *   cache_seqlens int32 [B] (device; 0 <= len <= 64 * max_pages_per_seq)
  *   O bf16 [B, s_q, H, d_c] (written)    LSE fp32 [B, s_q, H] (written)
- *   page_size = 64, d_c = 512, d_r = 64, H = 128, B >= 1, s_q >= 1,
+ *   page_size = 64, d_c = 512, d_r = 64, 1 <= H <= 128, B >= 1, s_q >= 1,
  *   num_pages >= 1, max_pages_per_seq >= 1, scale finite and > 0.
  *   workspace: device buffer of at least mla_decode_paged_workspace_bytes(B,
  *   s_q, H, d_c) bytes, 16-byte aligned, owned by the caller, overwritten; calls

@@ -81,7 +81,7 @@ def test_mla_decode_argument_errors(lib):
                               ctypes.c_float(scale), vp(ws), wsb, None)
     assert mla(N_kv=0) == 1
     assert mla(scale=-1.0) == 1
-    assert mla(H=64) == 2
+    assert mla(H=256) == 2                         # more than one 128-row tile of heads
     assert mla(d_c=256) == 2
     assert mla(Qn=0) == 1
     assert mla(Qn=40) == 3
@@ -99,7 +99,7 @@ def test_mla_decode_paged_argument_errors(lib):
     assert paged(num_pages=0) == 1
     assert paged(scale=0.0) == 1
     assert paged(page=32) == 2                     # page size other than 64
-    assert paged(H=64) == 2
+    assert paged(H=256) == 2
     assert paged(table=0) == 1                     # null block table
     assert paged(lens=18) == 3                     # misaligned lengths
     assert paged(Qn=40) == 3
@@ -145,7 +145,7 @@ def test_host_buffer_entry_point_argument_errors(lib):
         return lib.mla_decode_host(vp(Qn), vp(16), vp(16), vp(16), vp(16), vp(16), B, H, N_kv, 512, 64,
                                    ctypes.c_float(scale), vp(buf), nbytes, None)
     assert mla(B=0) == 1
-    assert mla(H=64) == 2
+    assert mla(H=256) == 2                         # more than one 128-row tile of heads
     assert mla(scale=0.0) == 1
     assert mla(Qn=0) == 1
     assert mla(buf=0) == 4

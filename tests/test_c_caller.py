@@ -34,7 +34,7 @@ int main(void)
                   GBATTN_ERR_UNSUPPORTED);
     bad |= expect("attn_fwd H % H_kv", attn_fwd(p, p, p, p, (float *)p, 1, 3, 2, 8, 8, 128, 0, 0, 0.1f, NULL),
                   GBATTN_ERR_INVALID_ARG);
-    bad |= expect("mla_decode H=64", mla_decode(p, p, p, p, p, (float *)p, 1, 64, 64, 512, 64, 0.04f, p, 0, NULL),
+    bad |= expect("mla_decode H=256", mla_decode(p, p, p, p, p, (float *)p, 1, 256, 64, 512, 64, 0.04f, p, 0, NULL),
                   GBATTN_ERR_UNSUPPORTED);
     bad |= expect("ssd_scan P=32", ssd_scan(p, (const float *)p, (const float *)p, p, p, NULL, (float *)p, NULL,
                                             1, 8, 2, 32, 1, 128, NULL),

@@ -36,6 +36,17 @@ def test_parity(B, N_kv):
     compare(O, LSE, O_ref, L_ref, what=f"B={B} N_kv={N_kv}")
 
 
+@pytest.mark.parametrize("H,B,N_kv", [(64, 3, 1000), (32, 70, 200), (16, 2, 4097), (100, 5, 777), (1, 4, 300),
+                                      (64, 1, 20000)])
+def test_fewer_heads(H, B, N_kv):
+    # H < 128: the heads fill the first H rows of the 128-row tile, the rest read
+    # as zero and are not written
+    Qn, Qp, KV, Kp = wl.random_mla(B, H, N_kv, 512, 64, seed=H * 1000 + B * 7 + N_kv)
+    O, LSE = run(Qn, Qp, KV, Kp)
+    O_ref, L_ref = oracle.mla_decode(Qn, Qp, KV, Kp, SCALE)
+    compare(O, LSE, O_ref, L_ref, what=f"H={H} B={B} N_kv={N_kv}")
+
+
 def test_large_scores_force_rescaling():
     # Ramp the RoPE keys (they enter the scores only, not the values): the row
     # maximum keeps moving along the sequence while V stays N(0, 1).

@@ -133,3 +133,19 @@ def test_several_query_tokens(s_q, lens):
     O_ref, L_ref = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, SCALE)
     compare(O.reshape(-1, 128, 512), LSE.reshape(-1, 128), O_ref.reshape(-1, 128, 512), L_ref.reshape(-1, 128),
             what=f"s_q={s_q} lens={lens}")
+
+
+@pytest.mark.parametrize("H,s_q,lens", [(64, 2, [5, 70, 130, 1, 4097, 0]), (32, 4, [3, 2, 64, 65, 1000]),
+                                        (16, 8, [7, 300, 4, 129]), (64, 3, [2, 64, 65, 1000, 0]),
+                                        (16, 1, [1, 63, 64, 65, 5000]), (128, 2, [3, 130])])
+def test_packed_query_tokens(H, s_q, lens):
+    # s_q * H <= 128: all of a sequence's tokens share one 128-row tile (its keys
+    # are read once), each row masked to its token's keys; H = 64 with s_q = 3
+    # takes two tiles per sequence (two tokens, then one); lengths shorter than
+    # s_q leave the first tokens without keys.
+    Qn, Qp, KV, Kp, table, L = wl.random_mla_paged(H, lens, seed=H * 31 + s_q * 7 + len(lens), s_q=s_q)
+    O, LSE = run_paged(Qn, Qp, KV, Kp, table, L)
+    lead = (len(lens), s_q, H) if s_q > 1 else (len(lens), H)
+    assert O.shape == (*lead, 512) and LSE.shape == lead
+    O_ref, L_ref = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, SCALE)
+    compare(O, LSE, O_ref, L_ref, what=f"H={H} s_q={s_q} lens={lens}")

@@ -309,8 +309,8 @@ extern "C" int mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_l
     if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0)
         return fail(GBATTN_ERR_INVALID_ARG, "mla_decode: need B, H, N_kv, d_c >= 1 and d_r >= 0");
     if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode: scale must be finite and > 0");
-    if (d_c != 512 || d_r != 64 || H != 128)
-        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode: supports d_c = 512, d_r = 64, H = 128");
+    if (d_c != 512 || d_r != 64 || H > 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode: supports d_c = 512, d_r = 64, H <= 128");
     if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode: problem too large");
     if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)
@@ -341,8 +341,8 @@ extern "C" int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const vo
         return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_noalloc: need B, H, N_kv, d_c >= 1 and d_r >= 0");
     if (!valid_scale(scale))
         return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_noalloc: scale must be finite and > 0");
-    if (d_c != 512 || d_r != 64 || H != 128)
-        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_noalloc: supports d_c = 512, d_r = 64, H = 128");
+    if (d_c != 512 || d_r != 64 || H > 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_noalloc: supports d_c = 512, d_r = 64, H <= 128");
     if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_noalloc: problem too large");
     if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)
@@ -379,8 +379,8 @@ extern "C" int mla_decode_paged(const void *Q_nope, const void *Q_pe, const void
         return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_paged: need B, s_q, H, num_pages, max_pages_per_seq, d_c, "
                                             "page_size >= 1 and d_r >= 0");
     if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_paged: scale must be finite and > 0");
-    if (d_c != 512 || d_r != 64 || H != 128 || page_size != 64)
-        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_paged: supports d_c = 512, d_r = 64, H = 128, page_size = 64");
+    if (d_c != 512 || d_r != 64 || H > 128 || page_size != 64)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_paged: supports d_c = 512, d_r = 64, H <= 128, page_size = 64");
     if (static_cast<long long>(B) * s_q * max_pages_per_seq > 0x7fffffffLL ||
         static_cast<long long>(max_pages_per_seq) * page_size > 0x7fffffffLL)
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_paged: problem too large");
@@ -624,8 +624,8 @@ extern "C" int mla_decode_host(const void *Q_nope, const void *Q_pe, const void 
     if (B < 1 || H < 1 || N_kv < 1 || d_c < 1 || d_r < 0)
         return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_host: need B, H, N_kv, d_c >= 1 and d_r >= 0");
     if (!valid_scale(scale)) return fail(GBATTN_ERR_INVALID_ARG, "mla_decode_host: scale must be finite and > 0");
-    if (d_c != 512 || d_r != 64 || H != 128)
-        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_host: supports d_c = 512, d_r = 64, H = 128");
+    if (d_c != 512 || d_r != 64 || H > 128)
+        return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_host: supports d_c = 512, d_r = 64, H <= 128");
     if (static_cast<long long>(N_kv) * d_c > (1LL << 31))
         return fail(GBATTN_ERR_UNSUPPORTED, "mla_decode_host: problem too large");
     if (!Q_nope || !Q_pe || !KV_latent || !K_pe || !O || !LSE)

@@ -110,10 +110,14 @@ struct Params {
     // Paged form only (sequences of their own lengths, 64-key pages):
     const int *tile_start;    // [B + 1] first flat tile of each sequence; tile_start[B] = all tiles
     const int *seq_len;       // [B] keys of each sequence (clamped to the block table's capacity)
-    const int *block_table;   // [B / q_per_seq][max_pages] page of each 64-key tile
+    const int *block_table;   // [sequences][max_pages] page of each 64-key tile
     int max_pages;
-    int q_per_seq;            // query tokens per sequence: entry b is token b % q_per_seq of
-                              // sequence b / q_per_seq (B counts (sequence, token) pairs)
+    // Work entries: B counts entries; an entry is up to 128 query rows of one
+    // sequence that share its keys.  A sequence has s_q query tokens of H heads
+    // (its query rows are [s_q][H], token-major); an entry takes tpe
+    // consecutive tokens (tpe = max(1, 128 / H)), so a sequence has epb =
+    // ceil(s_q / tpe) entries: entry e is group e % epb of sequence e / epb.
+    int H, s_q, tpe, epb;
     int max_seg;        // workspace slots per cluster (2: its first and last range)
     float c;            // scale * log2(e)
     int *status;
@@ -124,6 +128,22 @@ struct Params {
 __host__ __device__ __forceinline__ long long range_start(long long cl, long long T, int C)
 {
     return cl * T / C;
+}
+
+// Entry geometry (see Params): the sequence, the first query token, the
+// number of tokens and the first query row (within the sequence's s_q * H
+// rows) of entry e.
+struct Entry {
+    int seq, t0, nt, row0;
+};
+__host__ __device__ __forceinline__ Entry entry_of(int e, const Params &p)
+{
+    Entry x;
+    x.seq = e / p.epb;
+    x.t0 = (e % p.epb) * p.tpe;
+    x.nt = min(p.tpe, p.s_q - x.t0);
+    x.row0 = x.t0 * p.H;
+    return x;
 }
 
 // The cluster whose range holds flat tile x.
@@ -285,10 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const long long P0 = S.start(b);
                 const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
                 if (x0 >= x1) continue;       // an empty sequence
-                const int *pages =
-                    kPaged ? p.block_table + static_cast<size_t>(b / p.q_per_seq) * p.max_pages : nullptr;
+                const Entry en = entry_of(b, p);
+                const int *pages = kPaged ? p.block_table + static_cast<size_t>(en.seq) * p.max_pages : nullptr;
                 // paged: the page of the next tile, loaded one tile ahead of its use
-                int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : b;
+                int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : en.seq;
                 // This sequence's query part: two ring slots, each [128 heads x 64 dims]
                 // chunks 2i and 2i + 1 of Q_nope (one request), plus heads [64i, 64i + 64)
                 // of Q_pe on CTA 1.
@@ -299,25 +319,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], qbytes);
-                    tma_load_4d(dst, &tmQn, &c.full[s], 0, 0, chunk0 + 2 * qi, b);
-                    if (rank == 1) tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], 0, qi * 64, b);
+                    tma_load_4d(dst, &tmQn, &c.full[s], 0, en.row0, chunk0 + 2 * qi, en.seq);
+                    if (rank == 1) tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], 0, en.row0 + qi * 64, en.seq);
                 }
                 for (long long x = x0; x < x1 && ok; ++x, ++it) {
                     if (mine == 0 && x == max(x0, x1 - 4) && b < b_last) {
                         // The next range's query and first key tiles into L2 a few tiles
                         // ahead: its two query slots take half the ring, so its first
                         // tile is loaded late and must not also pay the HBM latency.
-                        const int nb = S.of_tile(x1);          // the next sequence with tiles here
-                        tma_prefetch_l2_4d(&tmQn, 0, 0, chunk0, nb);
+                        const int nb = S.of_tile(x1);          // the next entry with tiles here
+                        const Entry ne = entry_of(nb, p);
+                        tma_prefetch_l2_4d(&tmQn, 0, ne.row0, chunk0, ne.seq);
                         if (rank == 1) {
-                            tma_prefetch_l2_3d(&tmQp, 0, 0, nb);
-                            tma_prefetch_l2_3d(&tmQp, 0, 64, nb);
+                            tma_prefetch_l2_3d(&tmQp, 0, ne.row0, ne.seq);
+                            tma_prefetch_l2_3d(&tmQp, 0, ne.row0 + 64, ne.seq);
                         }
                         const long long nn = min(S.start(nb + 1), t_end) - x1;
                         for (int j = 0; j < min(nn, 3LL); ++j) {
                             const int r = kPaged ? 0 : j * kBN;
-                            const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(nb / p.q_per_seq) * p.max_pages + j)
-                                                 : nb;
+                            const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(ne.seq) * p.max_pages + j)
+                                                 : ne.seq;
                             tma_prefetch_l2_4d(&tmKV, 0, r, chunk0, o);
                             if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, r, o);
                         }
@@ -603,6 +624,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int n = static_cast<int>(x1 - x0);
             if (n <= 0) continue;         // an empty sequence
             const int n_keys = S.keys(b);
+            const Entry en = entry_of(b, p);
+            // This row's keys: the entry's key count less one per later token of
+            // the entry (token t of a sequence sees keys < len - (s_q - 1 - t));
+            // rows past the entry's tokens are not written and see every key.
+            const int nrows = en.nt * p.H;
+            const int row_keys = row < nrows ? n_keys - (en.nt - 1 - row / p.H) : n_keys;
             ++seg;
             float m_ref = -INFINITY, l = 0.f;
             for (int i = 0; i < n && ok; ++i, ++t) {
@@ -631,10 +658,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
 
                     const int key0 = static_cast<int>(x0 + i - P0) * kBN + h * kBU;
-                    if (key0 + kBU > n_keys) {
+                    if (key0 + kBU > row_keys) {
 #pragma unroll
                         for (int k = 0; k < kBU; ++k)
-                            if (key0 + k >= n_keys) s[k] = -INFINITY;
+                            if (key0 + k >= row_keys) s[k] = -INFINITY;
                     }
                     float m4[4];
 #pragma unroll
@@ -692,10 +719,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             const float lse = l > 0.f ? (m_ref * cexp + __log2f(l)) * kLn2 : -INFINITY;
             const size_t slot = static_cast<size_t>(cl) * 2 + (b == b_first ? 0 : 1);
-            // O / l of this range, bf16, to the final output (a whole sequence)
-            // or to the workspace slot (a part of a split sequence).
-            __nv_bfloat16 *obase = whole ? p.O + (static_cast<size_t>(b) * kH + row) * kDc + dim0
-                                         : p.ws_O + (slot * kH + row) * kDc + dim0;
+            // O / l of this range, bf16, to the final output (a whole entry)
+            // or to the workspace slot (a part of a split entry).
+            const size_t orow = static_cast<size_t>(en.seq) * p.s_q * p.H + en.row0 + row;
+            const bool store = !whole || row < nrows;
+            __nv_bfloat16 *obase = whole ? p.O + orow * kDc + dim0 : p.ws_O + (slot * kH + row) * kDc + dim0;
 #pragma unroll 1
             for (int ch = 0; ch < kHalf / 32; ++ch) {
                 uint32_t o[32];
@@ -706,12 +734,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 16; ++k)
                     w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
                 uint4 *dst = reinterpret_cast<uint4 *>(obase + ch * 32);
+                if (store) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                    for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                }
             }
-            if (rank == 0) {
+            if (rank == 0 && store) {
                 if (whole)
-                    p.LSE[static_cast<size_t>(b) * kH + row] = lse;
+                    p.LSE[orow] = lse;
                 else
                     p.ws_LSE[slot * kH + row] = lse;
             }
@@ -745,15 +775,18 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the split kernel is complete
     const SeqMap<kPaged> S{p};
     const int b = blockIdx.x / 8, hg = blockIdx.x % 8;
-    const int h = hg * 16 + threadIdx.x / 16;
+    const int h = hg * 16 + threadIdx.x / 16;        // the entry's row
     const int d0 = (threadIdx.x % 16) * 32;
+    const Entry en = entry_of(b, p);
+    if (h >= en.nt * p.H) return;                    // not a query row of this entry
+    const size_t orow = static_cast<size_t>(en.seq) * p.s_q * p.H + en.row0 + h;
     const long long T = S.total();
     const long long x0 = S.start(b), x1 = S.start(b + 1);
     if (x1 <= x0) {
-        uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * kH + h) * kDc + d0);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.O + orow * kDc + d0);
 #pragma unroll
         for (int k = 0; k < 4; ++k) dst[k] = make_uint4(0, 0, 0, 0);
-        if (threadIdx.x % 16 == 0) p.LSE[static_cast<size_t>(b) * kH + h] = -INFINITY;
+        if (threadIdx.x % 16 == 0) p.LSE[orow] = -INFINITY;
         return;
     }
     const int Ce = static_cast<int>(min(static_cast<long long>(p.C), T));   // clusters with work
@@ -821,20 +854,21 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     uint32_t *o = reinterpret_cast<uint32_t *>(out);
 #pragma unroll
     for (int k = 0; k < 16; ++k) o[k] = pack_bf16x2(acc[2 * k], acc[2 * k + 1]);
-    uint4 *dst = reinterpret_cast<uint4 *>(p.O + (static_cast<size_t>(b) * kH + h) * kDc + d0);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.O + orow * kDc + d0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) dst[k] = out[k];
-    if (threadIdx.x % 16 == 0) p.LSE[static_cast<size_t>(b) * kH + h] = lse;
+    if (threadIdx.x % 16 == 0) p.LSE[orow] = lse;
 }
 
-// Paged form: the key count of every (sequence, query token) entry b (token
-// t = b % s_q of sequence b / s_q sees keys < len - (s_q - 1 - t); lengths
-// outside [0, capacity] are clamped and set the status word) and the
-// exclusive prefix sum of their 64-key tile counts, tile_start[0..B].  One
-// block.
+// Paged form: the key count of every entry b (the keys its last token sees:
+// token t of a sequence sees keys < len - (s_q - 1 - t); lengths outside
+// [0, capacity] are clamped and set the status word) and the exclusive prefix
+// sum of their 64-key tile counts, tile_start[0..B].  One block.
 __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlens, int *seq_len, int *tile_start,
-                                                        int B, int s_q, int capacity, int *status)
+                                                        Params p, int capacity)
 {
+    const int B = p.B, s_q = p.s_q;
+    int *status = p.status;
     __shared__ int warp_sum[32];
     __shared__ int carry;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -845,12 +879,13 @@ __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlen
         const int b = base + threadIdx.x;
         int n = 0;
         if (b < B) {
-            int len = cache_seqlens[b / s_q];
+            const Entry en = entry_of(b, p);
+            int len = cache_seqlens[en.seq];
             if (len < 0 || len > capacity) {
-                if (b % s_q == 0) atomicCAS(status, 0, kStatusBadLength);
+                if (en.t0 == 0) atomicCAS(status, 0, kStatusBadLength);
                 len = min(max(len, 0), capacity);
             }
-            len = max(len - (s_q - 1 - b % s_q), 0);
+            len = max(len - (s_q - en.t0 - en.nt), 0);
             seq_len[b] = len;
             n = (len + kBN - 1) / kBN;
         }
@@ -1004,9 +1039,15 @@ int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *
                              kNoAllocScratchBytes, env, err);
 }
 
+// Tokens of one sequence that share a 128-row entry (1 when H = 128).
+static int tokens_per_entry(int H)
+{
+    return std::max(1, kH / H);
+}
+
 size_t mla_workspace_bytes(int B, int H, int N_kv, int d_c, int num_sms)
 {
-    if (B < 1 || H != kH || N_kv < 1 || d_c != kDc) return 0;
+    if (B < 1 || H < 1 || H > kH || N_kv < 1 || d_c != kDc) return 0;
     return plan_bytes(make_plan(B, N_kv, resident_clusters(num_sms)));
 }
 
@@ -1022,15 +1063,19 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     CUtensorMap tkv, tkp, tqn, tqp;
     if (!make_tma_bf16_chunked(tkv, KV_latent, d_c, N_kv, B, kBN, 4, err) ||
         !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
-        !make_tma_bf16_chunked(tqn, Q_nope, d_c, kH, B, kH, 2, err) ||
-        !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
+        !make_tma_bf16_chunked(tqn, Q_nope, d_c, H, B, kH, 2, err) ||
+        !make_tma_bf16_3d(tqp, Q_pe, d_r, H, B, kH / 2, err))
         return 5;
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
     p.ws_O = static_cast<__nv_bfloat16 *>(workspace);
     p.ws_LSE = reinterpret_cast<float *>(p.ws_O + pl.slots * kH * kDc);
-    p.B = B;
+    p.B = B;                  // one entry per sequence (one query token of H <= 128 heads)
+    p.H = H;
+    p.s_q = 1;
+    p.tpe = tokens_per_entry(H);
+    p.epb = 1;
     p.N_kv = N_kv;
     p.ntile = pl.ntile;
     p.T = pl.T;
@@ -1043,7 +1088,6 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     p.seq_len = nullptr;
     p.block_table = nullptr;
     p.max_pages = 0;
-    p.q_per_seq = 1;
     cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e == cudaSuccess) {
@@ -1073,7 +1117,7 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
 
 // ---------------------------------------------------------------- paged form
 // Workspace: split partials as in the dense form (2 slots per cluster), then
-// tile_start [B + 1] and seq_len [B] (int32).
+// tile_start [E + 1] and seq_len [E] (int32) for the E entries.
 static size_t paged_bytes(int B, int clusters, size_t &off_tiles)
 {
     const size_t slots = static_cast<size_t>(clusters) * 2;
@@ -1081,11 +1125,18 @@ static size_t paged_bytes(int B, int clusters, size_t &off_tiles)
     return off_tiles + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
 }
 
+// Entries of B sequences of s_q tokens of H heads.
+static long long paged_entries(int B, int s_q, int H)
+{
+    const int tpe = tokens_per_entry(H);
+    return static_cast<long long>(B) * ((s_q + tpe - 1) / tpe);
+}
+
 size_t mla_paged_workspace_bytes(int B, int s_q, int H, int d_c, int num_sms)
 {
-    if (B < 1 || s_q < 1 || H != kH || d_c != kDc) return 0;
+    if (B < 1 || s_q < 1 || H < 1 || H > kH || d_c != kDc) return 0;
     size_t off = 0;
-    return paged_bytes(B * s_q, resident_clusters(num_sms), off);
+    return paged_bytes(static_cast<int>(paged_entries(B, s_q, H)), resident_clusters(num_sms), off);
 }
 
 int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV_cache, const void *K_pe_cache,
@@ -1093,7 +1144,9 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
                             int s_q, int H, int num_pages, int max_pages, int d_c, int d_r, float scale,
                             void *workspace, size_t workspace_bytes, const LaunchEnv &env, std::string &err)
 {
-    const int B = B_seq * s_q;           // (sequence, query token) entries
+    const int tpe = tokens_per_entry(H);
+    const int epb = (s_q + tpe - 1) / tpe;
+    const int B = static_cast<int>(paged_entries(B_seq, s_q, H));   // entries
     const int C = resident_clusters(env.num_sms);
     size_t off_tiles = 0;
     if (workspace_bytes < paged_bytes(B, C, off_tiles)) {
@@ -1103,8 +1156,8 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
     CUtensorMap tkv, tkp, tqn, tqp;
     if (!make_tma_bf16_chunked(tkv, KV_cache, d_c, kBN, num_pages, kBN, 4, err) ||
         !make_tma_bf16_3d(tkp, K_pe_cache, d_r, kBN, num_pages, kBN, err) ||
-        !make_tma_bf16_chunked(tqn, Q_nope, d_c, kH, B, kH, 2, err) ||
-        !make_tma_bf16_3d(tqp, Q_pe, d_r, kH, B, kH / 2, err))
+        !make_tma_bf16_chunked(tqn, Q_nope, d_c, static_cast<uint64_t>(s_q) * H, B_seq, kH, 2, err) ||
+        !make_tma_bf16_3d(tqp, Q_pe, d_r, static_cast<uint64_t>(s_q) * H, B_seq, kH / 2, err))
         return 5;
     const size_t slots = static_cast<size_t>(C) * 2;
     Params p;
@@ -1127,9 +1180,11 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
     p.seq_len = seq_len;
     p.block_table = block_table;
     p.max_pages = max_pages;
-    p.q_per_seq = s_q;
-    mla_tiles_kernel<<<1, 1024, 0, env.stream>>>(cache_seqlens, seq_len, tile_start, B, s_q, max_pages * kBN,
-                                                 env.status);
+    p.H = H;
+    p.s_q = s_q;
+    p.tpe = tpe;
+    p.epb = epb;
+    mla_tiles_kernel<<<1, 1024, 0, env.stream>>>(cache_seqlens, seq_len, tile_start, p, max_pages * kBN);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(mla_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
