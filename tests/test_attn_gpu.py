@@ -145,9 +145,27 @@ def test_workload_mha_causal_2k_full():
     _workload_parity("mha_causal_b4_h16_n2048_d128", 0, full=True)
 
 
-@pytest.mark.parametrize("name", ["gqa_causal_b2_h32_hkv8_n8192_d128",
-                                  "gqa_window256_b2_h32_hkv8_n8192_d128",
-                                  "gqa_swindow256_b2_h32_hkv8_n8192_d128",
-                                  "mha_causal_spiky_b1_h32_n16384_d128"])
+FULL_SIZE = ["gqa_causal_b2_h32_hkv8_n8192_d128",
+             "gqa_window256_b2_h32_hkv8_n8192_d128",
+             "gqa_swindow256_b2_h32_hkv8_n8192_d128",
+             "mha_causal_spiky_b1_h32_n16384_d128"]
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
 def test_workload_sampled(name):
     _workload_parity(name, 160)
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_workload_complete_heads(name):
+    # Every row of two whole (batch, head) pairs of the full-size launch: the
+    # last head, whose shortest query blocks are the last CTAs of the
+    # longest-first order, and one in the middle of the grid.
+    c = wl.WORKLOADS[name]
+    Q, K, V = wl.prefill_inputs(c)
+    O, LSE = run_gpu(Q, K, V, c.causal, c.window, c.softmax_scale())
+    heads = [c.B * c.H - 1, (c.B * c.H) // 2 + 1]
+    rows = np.concatenate([np.arange(bh * c.N_q, (bh + 1) * c.N_q, dtype=np.int64) for bh in heads])
+    O_ref, L_ref = oracle.attn_fwd(Q, K, V, c.causal, c.window, c.softmax_scale(), rows=rows)
+    idx = torch.as_tensor(rows, device=O.device)
+    compare(O.reshape(-1, c.d)[idx], LSE.reshape(-1)[idx], O_ref, L_ref, what=f"{name} heads {heads}")

@@ -118,7 +118,10 @@ def test_varied_lengths_full_size_sampled():
     Qn, Qp, KV, Kp, table, L = wl.random_mla_paged(128, lens, seed=48)
     O, LSE = run_paged(Qn, Qp, KV, Kp, table, L)
     rng = np.random.default_rng(49)
-    rows = np.unique(np.concatenate([rng.integers(0, 64 * 128, 96), [0, 64 * 128 - 1]]))
+    # 96 random rows plus every head of three whole sequences (the first, one in
+    # the middle and the last, whose ranges end the last clusters' work)
+    rows = np.unique(np.concatenate([rng.integers(0, 64 * 128, 96), np.arange(0, 128), np.arange(31 * 128, 32 * 128),
+                                     np.arange(63 * 128, 64 * 128)]))
     O_ref, L_ref = oracle.mla_decode_paged(Qn, Qp, KV, Kp, table, L, SCALE, rows=rows)
     idx = torch.as_tensor(rows, device=O.device)
     compare(O.reshape(-1, 512)[idx], LSE.reshape(-1)[idx], O_ref, L_ref, what="64 varied sequences")
