@@ -53,6 +53,7 @@
 #include <cmath>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -80,6 +81,13 @@ constexpr int kQChunk = kH * 128;         // [128 heads x 64 dims] bf16, one TMA
 constexpr uint32_t kBarX = 1, kBarS = 2;  // named barriers of the sender / softmax warps
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
+// Split-KV partial results (O / l of a part of an entry's keys) are stored in
+// bf16 (true: fp32).  fp32 partials round the merged output once instead of
+// twice but double the partials' traffic: measured 13 % slower on 64
+// sequences of 4096 keys, where about 150 of the partials are written and
+// read back.
+constexpr bool kF32Partials = false;
+using PartT = std::conditional_t<kF32Partials, float, __nv_bfloat16>;
 
 struct Ctl {
     uint64_t q_full, q_empty;
@@ -102,7 +110,7 @@ static_assert(kStages % 2 == 0, "the two producer warps own alternate stages");
 struct Params {
     __nv_bfloat16 *O;
     float *LSE;
-    __nv_bfloat16 *ws_O;   // [slots][128][512] bf16, O / l of partial ranges
+    PartT *ws_O;        // [slots][128][512], O / l of partial ranges
     float *ws_LSE;      // [slots][128]
     int B, N_kv, ntile;
     long long T;        // B * ntile
@@ -136,9 +144,17 @@ __host__ __device__ __forceinline__ long long range_start(long long cl, long lon
 struct Entry {
     int seq, t0, nt, row0;
 };
+template <bool kPaged = true>
 __host__ __device__ __forceinline__ Entry entry_of(int e, const Params &p)
 {
     Entry x;
+    if constexpr (!kPaged) {      // dense form: one token of H <= 128 heads per sequence
+        x.seq = e;
+        x.t0 = 0;
+        x.nt = 1;
+        x.row0 = 0;
+        return x;
+    }
     x.seq = e / p.epb;
     x.t0 = (e % p.epb) * p.tpe;
     x.nt = min(p.tpe, p.s_q - x.t0);
@@ -305,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const long long P0 = S.start(b);
                 const long long x0 = max(t_begin, P0), x1 = min(t_end, S.start(b + 1));
                 if (x0 >= x1) continue;       // an empty sequence
-                const Entry en = entry_of(b, p);
+                const Entry en = entry_of<kPaged>(b, p);
                 const int *pages = kPaged ? p.block_table + static_cast<size_t>(en.seq) * p.max_pages : nullptr;
                 // paged: the page of the next tile, loaded one tile ahead of its use
                 int outer_next = kPaged ? __ldg(pages + (x0 - P0)) : en.seq;
@@ -328,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         // ahead: its two query slots take half the ring, so its first
                         // tile is loaded late and must not also pay the HBM latency.
                         const int nb = S.of_tile(x1);          // the next entry with tiles here
-                        const Entry ne = entry_of(nb, p);
+                        const Entry ne = entry_of<kPaged>(nb, p);
                         tma_prefetch_l2_4d(&tmQn, 0, ne.row0, chunk0, ne.seq);
                         if (rank == 1) {
                             tma_prefetch_l2_3d(&tmQp, 0, ne.row0, ne.seq);
@@ -624,12 +640,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int n = static_cast<int>(x1 - x0);
             if (n <= 0) continue;         // an empty sequence
             const int n_keys = S.keys(b);
-            const Entry en = entry_of(b, p);
+            const Entry en = entry_of<kPaged>(b, p);
             // This row's keys: the entry's key count less one per later token of
             // the entry (token t of a sequence sees keys < len - (s_q - 1 - t));
             // rows past the entry's tokens are not written and see every key.
             const int nrows = en.nt * p.H;
             const int row_keys = row < nrows ? n_keys - (en.nt - 1 - row / p.H) : n_keys;
+            const int min_keys = n_keys - (en.nt - 1);     // the entry's first token's keys (same for all rows)
             ++seg;
             float m_ref = -INFINITY, l = 0.f;
             for (int i = 0; i < n && ok; ++i, ++t) {
@@ -658,34 +675,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
 
                     const int key0 = static_cast<int>(x0 + i - P0) * kBN + h * kBU;
-                    if (key0 + kBU > row_keys) {
+                    if (key0 + kBU > min_keys) {            // a unit some row of the entry ends in
 #pragma unroll
                         for (int k = 0; k < kBU; ++k)
                             if (key0 + k >= row_keys) s[k] = -INFINITY;
                     }
-                    float m4[4];
+                    float mx = s[0];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        m4[q] = s[q];
-#pragma unroll
-                        for (int k = 4 + q; k < kBU; k += 4) m4[q] = fmaxf(m4[q], s[k]);
-                    }
-                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    for (int k = 1; k < kBU; ++k) mx = fmaxf(mx, s[k]);
                     const bool move = mx > m_ref + thr;
                     const float new_ref = move ? mx : m_ref;
                     const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
                     m_ref = new_ref;
                     const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-                    float sum2[2] = {0.f, 0.f};
+                    float sum = 0.f;
                     uint32_t pk[kBU / 2];
 #pragma unroll
                     for (int k = 0; k < kBU / 2; ++k) {
                         const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
                         const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
-                        sum2[k & 1] += p0 + p1;
+                        sum += p0 + p1;
                         pk[k] = pack_bf16x2(p0, p1);
                     }
-                    l = l * alpha + (sum2[0] + sum2[1]);
+                    l = l * alpha + sum;
                     // P buffer h was read by the MMA of unit (t - 1, h).
                     if (t > 0) okw = __all_sync(0xffffffffu, mbar_wait(&c.pfree[h], (t - 1) & 1u, ctl)) && okw;
                     // O must hold every earlier unit of this range before it is rescaled.
@@ -723,20 +735,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // or to the workspace slot (a part of a split entry).
             const size_t orow = static_cast<size_t>(en.seq) * p.s_q * p.H + en.row0 + row;
             const bool store = !whole || row < nrows;
-            __nv_bfloat16 *obase = whole ? p.O + orow * kDc + dim0 : p.ws_O + (slot * kH + row) * kDc + dim0;
+            __nv_bfloat16 *obase = p.O + orow * kDc + dim0;
+            PartT *pbase = p.ws_O + (slot * kH + row) * kDc + dim0;
 #pragma unroll 1
             for (int ch = 0; ch < kHalf / 32; ++ch) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + ch * 32, o);
-                uint4 v[4];
-                uint32_t *w = reinterpret_cast<uint32_t *>(v);
+                if (whole || !kF32Partials) {
+                    uint4 v[4];
+                    uint32_t *w = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-                uint4 *dst = reinterpret_cast<uint4 *>(obase + ch * 32);
-                if (store) {
+                    for (int k = 0; k < 16; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                    uint4 *dst = whole ? reinterpret_cast<uint4 *>(obase + ch * 32)
+                                       : reinterpret_cast<uint4 *>(pbase + ch * 32);
+                    if (store) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                        for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(pbase + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                             __uint_as_float(o[4 * k + 2]) * inv_l,
+                                             __uint_as_float(o[4 * k + 3]) * inv_l);
                 }
             }
             if (rank == 0 && store) {
@@ -763,12 +786,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
-// Merge the parts of each split sequence: LSE = ln sum_q e^{LSE_q},
-// O = sum_q e^{LSE_q - LSE} (O_q / l_q).  One block per (sequence, group of 16
-// heads), 256 threads, 32 output dims per thread; sequences written whole by
-// the split kernel are skipped, and (paged form) a sequence of length 0 gets
-// O = 0, LSE = -inf.  Up to three parts (the usual case) every load of a
-// thread is issued at once.
+// Merge the parts of each split entry: LSE = ln sum_q e^{LSE_q},
+// O = sum_q e^{LSE_q - LSE} (O_q / l_q).  One block per (entry, group of 16
+// rows), 256 threads, 32 output dims per thread; entries written whole by the
+// split kernel are skipped, and (paged form) an entry without keys gets
+// O = 0, LSE = -inf.
 template <bool kPaged>
 __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
 {
@@ -777,7 +799,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     const int b = blockIdx.x / 8, hg = blockIdx.x % 8;
     const int h = hg * 16 + threadIdx.x / 16;        // the entry's row
     const int d0 = (threadIdx.x % 16) * 32;
-    const Entry en = entry_of(b, p);
+    const Entry en = entry_of<kPaged>(b, p);
     if (h >= en.nt * p.H) return;                    // not a query row of this entry
     const size_t orow = static_cast<size_t>(en.seq) * p.s_q * p.H + en.row0 + h;
     const long long T = S.total();
@@ -796,14 +818,25 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     auto slot_of = [&](int q) -> size_t {
         return static_cast<size_t>(q) * 2 + (b == S.of_tile(range_start(q, T, Ce)) ? 0 : 1);
     };
-    auto accumulate = [](float (&acc)[32], float w, const uint4 (&v)[4]) {
+    // One part's 32 values of this thread: 4 (bf16) or 8 (fp32) 16-byte loads.
+    constexpr int kVec = kF32Partials ? 8 : 4;
+    auto load_part = [&](size_t sq, uint4 (&v)[kVec]) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.ws_O + (sq * kH + h) * kDc + d0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kVec; ++k) v[k] = src[k];
+    };
+    auto accumulate = [](float (&acc)[32], float w, const uint4 (&v)[kVec]) {
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
             const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                acc[8 * k + 2 * j] += w * __uint_as_float(u[j] << 16);
-                acc[8 * k + 2 * j + 1] += w * __uint_as_float(u[j] & 0xffff0000u);
+                if constexpr (kF32Partials) {
+                    acc[4 * k + j] += w * __uint_as_float(u[j]);
+                } else {
+                    acc[8 * k + 2 * j] += w * __uint_as_float(u[j] << 16);
+                    acc[8 * k + 2 * j + 1] += w * __uint_as_float(u[j] & 0xffff0000u);
+                }
             }
         }
     };
@@ -812,28 +845,31 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
     for (int k = 0; k < 32; ++k) acc[k] = 0.f;
     float lse;
     const int n = c1 - c0 + 1;
-    if (n <= 3) {
-        float lq[3];
-        uint4 v[3][4];
+    // Up to kPre parts (the usual case: an entry spans two or three cluster
+    // ranges) every load of the thread is issued at once.
+    constexpr int kPre = kF32Partials ? 2 : 3;
+    if (n <= kPre) {
+        float lq[kPre];
+        uint4 v[kPre][kVec];
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < kPre; ++i) {
             lq[i] = -INFINITY;
             if (i < n) {
                 const size_t sq = slot_of(c0 + i);
                 lq[i] = p.ws_LSE[sq * kH + h];
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.ws_O + (sq * kH + h) * kDc + d0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) v[i][k] = src[k];
+                load_part(sq, v[i]);
             }
         }
-        const float mx = fmaxf(fmaxf(lq[0], lq[1]), lq[2]);
+        float mx = lq[0];
+#pragma unroll
+        for (int i = 1; i < kPre; ++i) mx = fmaxf(mx, lq[i]);
         float denom = 0.f;
 #pragma unroll
-        for (int i = 0; i < 3; ++i)
+        for (int i = 0; i < kPre; ++i)
             if (i < n) denom += expf(lq[i] - mx);
         lse = mx + logf(denom);
 #pragma unroll
-        for (int i = 0; i < 3; ++i)
+        for (int i = 0; i < kPre; ++i)
             if (i < n) accumulate(acc, expf(lq[i] - lse), v[i]);
     } else {
         float mx = -INFINITY;
@@ -843,10 +879,8 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const Params p)
         lse = mx + logf(denom);
         for (int q = c0; q <= c1; ++q) {
             const size_t sq = slot_of(q);
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.ws_O + (sq * kH + h) * kDc + d0);
-            uint4 v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = src[k];
+            uint4 v[kVec];
+            load_part(sq, v);
             accumulate(acc, expf(p.ws_LSE[sq * kH + h] - lse), v);
         }
     }
@@ -879,7 +913,7 @@ __global__ void __launch_bounds__(1024) mla_tiles_kernel(const int *cache_seqlen
         const int b = base + threadIdx.x;
         int n = 0;
         if (b < B) {
-            const Entry en = entry_of(b, p);
+            const Entry en = entry_of<true>(b, p);
             int len = cache_seqlens[en.seq];
             if (len < 0 || len > capacity) {
                 if (en.t0 == 0) atomicCAS(status, 0, kStatusBadLength);
@@ -971,7 +1005,7 @@ Plan make_plan(int B, int N_kv, int clusters)
 
 size_t plan_bytes(const Plan &pl)
 {
-    return pl.slots * kH * kDc * sizeof(__nv_bfloat16) + pl.slots * kH * sizeof(float);
+    return pl.slots * kH * kDc * sizeof(PartT) + pl.slots * kH * sizeof(float);
 }
 
 // ---------------------------------------------------------------------------
@@ -988,7 +1022,7 @@ size_t plan_bytes(const Plan &pl)
 // GPU that loads the library holds it until the process exits.
 constexpr size_t kNoAllocMaxClusters = 80;
 constexpr size_t kNoAllocScratchBytes =
-    kNoAllocMaxClusters * 2 * (static_cast<size_t>(kH) * kDc * sizeof(__nv_bfloat16) + kH * sizeof(float));
+    kNoAllocMaxClusters * 2 * (static_cast<size_t>(kH) * kDc * sizeof(PartT) + kH * sizeof(float));
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 }  // namespace
@@ -1069,7 +1103,7 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-    p.ws_O = static_cast<__nv_bfloat16 *>(workspace);
+    p.ws_O = static_cast<PartT *>(workspace);
     p.ws_LSE = reinterpret_cast<float *>(p.ws_O + pl.slots * kH * kDc);
     p.B = B;                  // one entry per sequence (one query token of H <= 128 heads)
     p.H = H;
@@ -1121,7 +1155,7 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
 static size_t paged_bytes(int B, int clusters, size_t &off_tiles)
 {
     const size_t slots = static_cast<size_t>(clusters) * 2;
-    off_tiles = slots * kH * kDc * sizeof(__nv_bfloat16) + slots * kH * sizeof(float);
+    off_tiles = slots * kH * kDc * sizeof(PartT) + slots * kH * sizeof(float);
     return off_tiles + (2 * static_cast<size_t>(B) + 1) * sizeof(int);
 }
 
@@ -1163,7 +1197,7 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
-    p.ws_O = static_cast<__nv_bfloat16 *>(workspace);
+    p.ws_O = static_cast<PartT *>(workspace);
     p.ws_LSE = reinterpret_cast<float *>(p.ws_O + slots * kH * kDc);
     int *tile_start = reinterpret_cast<int *>(static_cast<char *>(workspace) + off_tiles);
     int *seq_len = tile_start + B + 1;
