@@ -214,6 +214,26 @@ bool make_tma_bf16_chunked(CUtensorMap &desc, const void *base, uint64_t cols, u
     return true;
 }
 
+bool make_tma_5d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[5], const uint64_t (&strides)[4],
+                 const uint32_t (&box)[5], std::string &err)
+{
+    if (!tensor_map_encoder()) {
+        err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    const cuuint64_t d[5] = {dims[0], dims[1], dims[2], dims[3], dims[4]};
+    const cuuint64_t st[4] = {strides[0], strides[1], strides[2], strides[3]};
+    const cuuint32_t bx[5] = {box[0], box[1], box[2], box[3], box[4]};
+    CUresult r = encode_cached(desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, d, st, bx);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for a 5-d bf16 map", static_cast<int>(r));
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
 bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
                  const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err)
 {

@@ -97,4 +97,9 @@ bool make_tma_bf16_chunked(CUtensorMap &desc, const void *base, uint64_t cols, u
 bool make_tma_4d(CUtensorMap &desc, bool f32, const void *base, const uint64_t (&dims)[4],
                  const uint64_t (&strides)[3], const uint32_t (&box)[4], std::string &err);
 
+// 5-D bf16 tensor map, 128-byte swizzle; dims innermost first, strides in
+// bytes of dims 1..4 (any order of sizes), box in elements.
+bool make_tma_5d(CUtensorMap &desc, const void *base, const uint64_t (&dims)[5], const uint64_t (&strides)[4],
+                 const uint32_t (&box)[5], std::string &err);
+
 }  // namespace gbattn

@@ -211,10 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *st = smem + u * kStageBytes;
                 mbar_arrive_expect_tx(&k.full[u], kStageBytes);
                 const int row = c * kQ;
-                tma_load_4d(st + kOffC, &tmC, &k.full[u], 0, g, row, b);
-                tma_load_4d(st + kOffC + kAtom, &tmC, &k.full[u], 64, g, row, b);
-                tma_load_4d(st + kOffB, &tmB, &k.full[u], 0, g, row, b);
-                tma_load_4d(st + kOffB + kAtom, &tmB, &k.full[u], 64, g, row, b);
+                // C and B: both 64-column halves of the chunk's rows in one request each
+                tma_load_5d(st + kOffC, &tmC, &k.full[u], 0, row, 0, g, b);
+                tma_load_5d(st + kOffB, &tmB, &k.full[u], 0, row, 0, g, b);
                 tma_load_4d(st + kOffX, &tmX, &k.full[u], 0, h, row, b);
                 // x of this head comes from HBM: ask for it two chunks ahead, so the
                 // load that refills this stage finds it in L2 (C and B are shared by
@@ -576,10 +575,6 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
         return 2;
     }
     CUtensorMap tc, tb, tx, ty;
-    const uint64_t bc_dims[4] = {static_cast<uint64_t>(kN), static_cast<uint64_t>(G), static_cast<uint64_t>(L),
-                                 static_cast<uint64_t>(Bsz)};
-    const uint64_t bc_strides[3] = {kN * 2ull, static_cast<uint64_t>(G) * kN * 2,
-                                    static_cast<uint64_t>(L) * G * kN * 2};
     const uint64_t x_dims[4] = {static_cast<uint64_t>(kP), static_cast<uint64_t>(H), static_cast<uint64_t>(L),
                                 static_cast<uint64_t>(Bsz)};
     const uint64_t x_strides[3] = {kP * 2ull, static_cast<uint64_t>(H) * kP * 2,
@@ -588,8 +583,15 @@ int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *
                                    static_cast<uint64_t>(L) * H * kP * 4};
     const uint32_t box[4] = {64, 1, kQ, 1};
     const uint32_t ybox[4] = {32, 1, 32, 1};
-    if (!make_tma_4d(tc, false, Cm, bc_dims, bc_strides, box, err) ||
-        !make_tma_4d(tb, false, Bm, bc_dims, bc_strides, box, err) ||
+    // C and B [Bsz][L][G][N] viewed as (64 columns, L, N / 64 halves, G, Bsz): the
+    // half index outside the row index, so one box lands as [half][row][64].
+    const uint64_t bc5_dims[5] = {64, static_cast<uint64_t>(L), static_cast<uint64_t>(kN / 64),
+                                  static_cast<uint64_t>(G), static_cast<uint64_t>(Bsz)};
+    const uint64_t bc5_strides[4] = {static_cast<uint64_t>(G) * kN * 2, 128, kN * 2ull,
+                                     static_cast<uint64_t>(L) * G * kN * 2};
+    const uint32_t bc5_box[5] = {64, kQ, kN / 64, 1, 1};
+    if (!make_tma_5d(tc, Cm, bc5_dims, bc5_strides, bc5_box, err) ||
+        !make_tma_5d(tb, Bm, bc5_dims, bc5_strides, bc5_box, err) ||
         !make_tma_4d(tx, false, x, x_dims, x_strides, box, err) ||
         !make_tma_4d(ty, true, y, x_dims, y_strides, ybox, err))
         return 5;
