@@ -218,11 +218,12 @@ int mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *KV_late
  * LSE in HOST memory (same shapes and layouts as attn_fwd; pinned memory
  * makes the copies asynchronous, pageable memory works but copies
  * synchronously).  The call copies the inputs to a caller-owned device
- * buffer, runs attn_fwd and copies O and LSE back, cut into up to 4
+ * buffer, runs attn_fwd and copies O and LSE back, cut into up to 8
  * contiguous chunks of (batch, KV-head) units so that the host-to-device
  * copies, the kernels and the device-to-host copies of different chunks
- * overlap (two library-owned helper streams per device, chained to `stream`
- * by events).  Asynchronous on `stream`: O and LSE are valid once `stream`
+ * overlap (library-owned helper streams per device, chained to `stream` by
+ * events; the chunks' kernels alternate between two of them, so consecutive
+ * chunks' kernels overlap too).  Asynchronous on `stream`: O and LSE are valid once `stream`
  * reaches the point of the call (e.g. after gbattn_check(stream)).
  *   device_buf: at least attn_fwd_host_device_bytes(B, H, H_kv, N_q, N_kv, d)
  *   bytes, 256-byte aligned, owned by the caller, overwritten.

@@ -455,19 +455,26 @@ extern "C" int ssd_scan(const void *x, const float *dt, const float *A, const vo
 // Host-buffer entry points: the same computation with inputs and outputs in
 // host memory.  The work is cut into a few contiguous chunks of (batch,
 // KV-head) units (each a valid problem on sub-tensors), and per chunk the
-// host-to-device copies (helper stream), the kernels (the caller's stream)
-// and the device-to-host copies (second helper stream) are chained by
-// events, so the copies of one chunk overlap the kernels and copies of the
-// others; the copies in alternate between two streams (two copy engines).  Pinned host memory gives asynchronous copies; pageable memory
-// works but copies synchronously.
+// host-to-device copies (two helper streams, two copy engines), the kernels
+// and the device-to-host copies (a third helper stream) are chained by events,
+// so the copies of one chunk overlap the kernels and copies of the others.
+// attn_fwd_host runs the chunks' kernels on two more helper streams, so that
+// one chunk's kernel starts while the previous one's last CTAs finish;
+// mla_decode_host runs them on the caller's stream (the chunks share one
+// split-KV workspace).  Pinned host memory gives asynchronous copies; pageable
+// memory works but copies synchronously.
 
 namespace {
-constexpr int kPipeChunks = 4;
+constexpr int kPipeChunks = 8;          // events per helper stream (the most chunks of any call)
+constexpr int kAttnChunks = 8;          // attn_fwd_host: chunks of (batch, KV-head) units
+constexpr int kMlaChunks = 4;           // mla_decode_host: chunks of sequences (fewer sequences per
+                                        // launch make the split-KV plan split more)
 
 struct HostPipe {
     std::mutex mu;            // held while a call enqueues (events are reused)
     bool init = false;
     cudaStream_t h2d[2] = {nullptr, nullptr}, d2h = nullptr;   // two copy-in streams: two copy engines
+    cudaStream_t kern[2] = {nullptr, nullptr};                 // attn_fwd_host's chunk kernels
     cudaEvent_t start = nullptr;
     cudaEvent_t ev_in[2][kPipeChunks], ev_k[kPipeChunks], ev_out = nullptr;
 };
@@ -479,10 +486,14 @@ int host_pipe(HostPipe *&hp)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(GBATTN_ERR_LAUNCH, "host pipeline: no device");
     hp = &g_pipe[dev];
+    static std::mutex init_mu;
+    std::lock_guard<std::mutex> lk(init_mu);
     if (hp->init) return GBATTN_OK;
     const unsigned ef = cudaEventDisableTiming;
     e = cudaStreamCreateWithFlags(&hp->h2d[0], cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->h2d[1], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->kern[0], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->kern[1], cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->start, ef);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_out, ef);
@@ -510,6 +521,7 @@ cudaError_t pipe_start(HostPipe *hp, cudaStream_t user)
 {
     cudaError_t e = cudaEventRecord(hp->start, user);
     for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(hp->h2d[j], hp->start, 0);
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(hp->kern[j], hp->start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->start, 0);
     return e;
 }
@@ -573,7 +585,7 @@ extern "C" int attn_fwd_host(const void *Q, const void *K, const void *V, void *
     uint8_t *dQ = static_cast<uint8_t *>(device_buf), *dK = dQ + round256(qb), *dV = dK + round256(kvb),
             *dO = dV + round256(kvb), *dL = dO + round256(qb);
     const int group = H / H_kv, units = B * H_kv;
-    const int nchunk = std::min(kPipeChunks, units);
+    const int nchunk = std::min(kAttnChunks, units);
     const size_t q_unit = static_cast<size_t>(group) * N_q * d * 2, kv_unit = static_cast<size_t>(N_kv) * d * 2,
                  l_unit = static_cast<size_t>(group) * N_q * 4;
     cudaError_t e = pipe_start(hp, env.stream);
@@ -587,23 +599,28 @@ extern "C" int attn_fwd_host(const void *Q, const void *K, const void *V, void *
                               nu * kv_unit},
                              {dV + u0 * kv_unit, V ? static_cast<const uint8_t *>(V) + u0 * kv_unit : nullptr,
                               nu * kv_unit}};
-        e = pipe_copy_in(hp, c, in, env.stream);
+        // this chunk's kernel on helper stream c % 2: it can start while the
+        // previous chunk's kernel drains on the other one
+        LaunchEnv kenv = env;
+        kenv.stream = hp->kern[c & 1];
+        e = pipe_copy_in(hp, c, in, kenv.stream);
         if (e != cudaSuccess) break;
         rc = launch_attn_fwd(dQ + u0 * q_unit, dK + u0 * kv_unit, dV + u0 * kv_unit, dO + u0 * q_unit,
                              reinterpret_cast<float *>(dL + u0 * l_unit), 1, nu * group, nu, N_q, N_kv, d, causal,
-                             window, scale, nullptr, env, err);
+                             window, scale, nullptr, kenv, err);
         if (rc != GBATTN_OK) {
             g_err = err;
             return rc;
         }
-        e = cudaEventRecord(hp->ev_k[c], env.stream);
+        e = cudaEventRecord(hp->ev_k[c], kenv.stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->ev_k[c], 0);
         const Piece out[2] = {{static_cast<uint8_t *>(O) + u0 * q_unit, dO + u0 * q_unit, nu * q_unit},
                               {reinterpret_cast<uint8_t *>(LSE) + u0 * l_unit, dL + u0 * l_unit, nu * l_unit}};
         for (const Piece &pc : out)
             if (e == cudaSuccess) e = cudaMemcpyAsync(pc.dst, pc.src, pc.bytes, cudaMemcpyDeviceToHost, hp->d2h);
     }
-    // the caller's stream continues once the last copy back is done
+    // the caller's stream continues once the last copy back is done (every
+    // chunk's copy back waited for that chunk's kernel)
     if (e == cudaSuccess) e = cudaEventRecord(hp->ev_out, hp->d2h);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(env.stream, hp->ev_out, 0);
     if (e != cudaSuccess) return fail(GBATTN_ERR_LAUNCH, std::string("attn_fwd_host: ") + cudaGetErrorString(e));
@@ -614,7 +631,7 @@ extern "C" int attn_fwd_host(const void *Q, const void *K, const void *V, void *
 // over the chunk sizes (the plan depends on the number of sequences).
 static size_t mla_host_chunk_workspace(int B, int H, int N_kv, int d_c, int num_sms)
 {
-    const int n = std::min(kPipeChunks, B);
+    const int n = std::min(kMlaChunks, B);
     size_t ws = 0;
     for (int c = 0; c < n; ++c) {
         const int nb = static_cast<int>(static_cast<long long>(c + 1) * B / n - static_cast<long long>(c) * B / n);
@@ -668,7 +685,7 @@ extern "C" int mla_decode_host(const void *Q_nope, const void *Q_pe, const void 
             *dKV = dQp + round256(B * qp_u), *dKp = dKV + round256(B * kv_u), *dO = dKp + round256(B * kp_u),
             *dL = dO + round256(B * o_u), *dW = dL + round256(B * l_u);
     const size_t ws_bytes = mla_host_chunk_workspace(B, H, N_kv, d_c, env.num_sms);
-    const int nchunk = std::min(kPipeChunks, B);
+    const int nchunk = std::min(kMlaChunks, B);
     cudaError_t e = pipe_start(hp, env.stream);
     std::string err;
     for (int c = 0; c < nchunk && e == cudaSuccess; ++c) {
