@@ -105,12 +105,13 @@ EncodeFn tensor_map_encoder()
 // the same buffers skip the driver's encode.  Bounded; cleared when full.
 struct MapKey {
     uintptr_t base;
-    int dtype, rank;
+    int dtype, rank, swizzle;
     uint64_t dims[5], strides[4];
     uint32_t box[5];
     bool operator==(const MapKey &o) const
     {
-        return base == o.base && dtype == o.dtype && rank == o.rank && std::equal(dims, dims + 5, o.dims) &&
+        return base == o.base && dtype == o.dtype && rank == o.rank && swizzle == o.swizzle &&
+               std::equal(dims, dims + 5, o.dims) &&
                std::equal(strides, strides + 4, o.strides) && std::equal(box, box + 5, o.box);
     }
 };
@@ -120,7 +121,8 @@ struct MapKeyHash {
         uint64_t h = 1469598103934665603ull;
         auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
         mix(k.base);
-        mix(static_cast<uint64_t>(k.dtype) << 8 | static_cast<uint64_t>(k.rank));
+        mix(static_cast<uint64_t>(k.dtype) << 16 | static_cast<uint64_t>(k.rank) << 8 |
+            static_cast<uint64_t>(k.swizzle));
         for (uint64_t v : k.dims) mix(v);
         for (uint64_t v : k.strides) mix(v);
         for (uint32_t v : k.box) mix(v);
@@ -131,14 +133,16 @@ constexpr size_t kMapCacheMax = 1024;
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// Encode (or fetch) a tiled, 128-byte-swizzled map; rank <= 5.
+// Encode (or fetch) a tiled map (128-byte swizzle unless given); rank <= 5.
 CUresult encode_cached(CUtensorMap &desc, CUtensorMapDataType dtype, int rank, const void *base,
-                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box)
+                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     MapKey key{};
     key.base = reinterpret_cast<uintptr_t>(base);
     key.dtype = static_cast<int>(dtype);
     key.rank = rank;
+    key.swizzle = static_cast<int>(swizzle);
     for (int i = 0; i < rank; ++i) {
         key.dims[i] = dims[i];
         key.box[i] = box[i];
@@ -156,7 +160,7 @@ CUresult encode_cached(CUtensorMap &desc, CUtensorMapDataType dtype, int rank, c
     if (!encode) return CUDA_ERROR_NOT_SUPPORTED;
     const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     CUresult r = encode(&desc, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base), dims, strides, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r == CUDA_SUCCESS) {
         std::lock_guard<std::mutex> lk(g_map_mu);
@@ -183,6 +187,29 @@ bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64
         snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu,%llu,%llu] box rows %u",
                  static_cast<int>(r), static_cast<unsigned long long>(outer),
                  static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols), box_rows);
+        err = buf;
+        return false;
+    }
+    return true;
+}
+
+bool make_tma_bf16_3d_sw64(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows, uint64_t outer,
+                           uint32_t box_rows, std::string &err)
+{
+    if (!tensor_map_encoder()) {
+        err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    const cuuint64_t dims[3] = {cols, rows, outer};
+    const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    const cuuint32_t box[3] = {32, box_rows, 1};
+    CUresult r = encode_cached(desc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_64B);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for a 64-byte-swizzled [%llu,%llu,%llu] map",
+                 static_cast<int>(r), static_cast<unsigned long long>(outer), static_cast<unsigned long long>(rows),
+                 static_cast<unsigned long long>(cols));
         err = buf;
         return false;
     }

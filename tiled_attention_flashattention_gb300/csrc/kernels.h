@@ -84,6 +84,10 @@ int launch_selftest_umma(const void *A, const void *B, const void *P, const void
 // Returns false and fills err on failure.
 bool make_tma_bf16_3d(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows,
                       uint64_t outer, uint32_t box_rows, std::string &err);
+// As make_tma_bf16_3d with boxes of 32 columns (64 bytes) x box_rows rows and
+// the 64-byte swizzle (for operands split into 32-dim halves).
+bool make_tma_bf16_3d_sw64(CUtensorMap &desc, const void *base, uint64_t cols, uint64_t rows, uint64_t outer,
+                           uint32_t box_rows, std::string &err);
 // The same row-major bf16 tensor [outer][rows][cols] (cols % 64 == 0) viewed
 // as 4-D (64 columns, rows, cols / 64, outer) with a box of 64 columns x
 // box_rows rows x box_chunks 64-column chunks: one load brings box_chunks

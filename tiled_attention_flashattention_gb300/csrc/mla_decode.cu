@@ -12,10 +12,10 @@
 // GB300 mapping.  The fp32 output accumulator of 128 heads x 512 latent dims
 // fills one SM's whole tensor memory, so a pair of CTAs (a 2-CTA cluster)
 // shares each work item and splits both the contraction and the output:
-//   CTA 0 holds latent dims [0, 256): its Q part and KV tiles cover those
-//         dims; it computes the partial score over them and owns O[:, 0:256);
-//   CTA 1 holds latent dims [256, 512) plus the 64 RoPE dims, computes the
-//         partial score over those 320 dims and owns O[:, 256:512).
+//   CTA r holds latent dims [256 r, 256 r + 256) and RoPE dims [32 r, 32 r + 32):
+//         its Q part and key tiles cover those 288 dims; it computes the
+//         partial score over them and owns O[:, 256 r : 256 r + 256).
+// (The RoPE halves are 64-byte rows, loaded and read with the 64-byte swizzle.)
 // Every KV byte is read from HBM by exactly one CTA.  The two fp32 partial
 // score tiles are swapped in 32-key units (128 heads x 32 keys, 16 KB) with
 // one bulk copy per CTA per unit (TMA engine, shared memory to the peer's
@@ -49,7 +49,7 @@
 //   warps 8-11  softmax (one thread per head): own + peer partial scores,
 //               online softmax, P (bf16) into TMEM, O rescaling, epilogue.
 // TMEM: O half [0, 256), S [256, 320), P [320, 352) (two 16-column units),
-// Q part [352, 512).
+// Q part [352, 496).
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -67,8 +67,9 @@ constexpr int kBU = 32;                   // keys per unit (exchange, softmax, P
 constexpr int kDc = 512;
 constexpr int kHalf = 256;                // latent dims owned by one CTA
 constexpr int kKvChunk = kBN * 128;       // [64 keys x 64 dims] bf16, one TMA box
-constexpr int kMaxChunks = 5;             // contraction chunks of CTA 1 (4 latent + RoPE)
-constexpr int kStageBytes = kMaxChunks * kKvChunk;
+constexpr int kRopeBytes = kBN * 64;      // [64 keys x 32 dims] bf16: this CTA's RoPE half of a key tile
+constexpr int kStageBytes = 4 * kKvChunk + kRopeBytes;   // 4 latent chunks + the RoPE half (36 KB)
+constexpr int kSSteps = 18;               // 16-dim K-steps of a CTA's score part (256 latent + 32 RoPE dims)
 constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
@@ -78,6 +79,8 @@ constexpr uint32_t kColP = 320;
 constexpr uint32_t kColQ = 352;
 constexpr int kXBytes = kH * kBU * 4;     // one unit of partial scores (fp32, 128-byte rows)
 constexpr int kQChunk = kH * 128;         // [128 heads x 64 dims] bf16, one TMA box of Q_nope
+constexpr int kQpeBytes = 64 * 64;        // [64 heads x 32 dims] bf16, one TMA box of Q_pe (64-byte swizzle)
+static_assert(2 * kQChunk + kQpeBytes <= kStageBytes, "a query slot fits a ring stage");
 constexpr uint32_t kBarX = 1, kBarS = 2;  // named barriers of the sender / softmax warps
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
@@ -220,14 +223,16 @@ __device__ __forceinline__ void bulk_wait_read_allow1()
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
-// S_part = Q_part K_part^T over NK 16-dim steps: A = Q from TMEM (8 columns
-// per step), B = the stage's 64-dim chunks (K-major, 32 bytes per step).
-template <int NK>
-__device__ __forceinline__ void issue_s(uint32_t d, uint32_t a, uint64_t kvd, uint32_t idesc)
+// S_part = Q_part K_part^T over the 18 16-dim steps of this CTA's part: A = Q
+// from TMEM (8 columns per step), B = the stage's latent chunks (K-major,
+// 128-byte swizzle, 32 bytes per step) and then its RoPE half (64-byte swizzle).
+__device__ __forceinline__ void issue_s(uint32_t d, uint32_t a, uint64_t kvd, uint64_t rpd, uint32_t idesc)
 {
 #pragma unroll
-    for (int k = 0; k < NK; ++k)
+    for (int k = 0; k < 16; ++k)
         umma_ts(d, a + k * 8, desc_advance(kvd, (k / 4) * kKvChunk + (k % 4) * 32), idesc, k > 0 ? 1u : 0u);
+#pragma unroll
+    for (int k = 16; k < kSSteps; ++k) umma_ts(d, a + k * 8, desc_advance(rpd, (k - 16) * 32), idesc, 1u);
 }
 
 template <bool kPaged>
@@ -247,7 +252,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int cl = blockIdx.x / 2;
-    const int nch = rank == 0 ? 4 : 5;              // contraction chunks of this CTA
     const int dim0 = static_cast<int>(rank) * kHalf;
 
     if (threadIdx.x == 0) {
@@ -314,8 +318,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             int it = 0;
-            const uint32_t kvbytes = nch * kKvChunk;
-            const uint32_t qbytes = rank == 0 ? 2 * kQChunk : 2 * kQChunk + kQChunk / 2;
+            const uint32_t kvbytes = kStageBytes;
+            const uint32_t qbytes = 2 * kQChunk + kQpeBytes;
+            const int rope0 = static_cast<int>(rank) * 32;                  // this CTA's RoPE dims
             const int chunk0 = static_cast<int>(rank) * (kHalf / 64);     // this CTA's first latent chunk
             for (int b = b_first; b <= b_last && ok; ++b) {
                 const long long P0 = S.start(b);
@@ -336,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], qbytes);
                     tma_load_4d(dst, &tmQn, &c.full[s], 0, en.row0, chunk0 + 2 * qi, en.seq);
-                    if (rank == 1) tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], 0, en.row0 + qi * 64, en.seq);
+                    tma_load_3d(dst + 2 * kQChunk, &tmQp, &c.full[s], rope0, en.row0 + qi * 64, en.seq);
                 }
                 for (long long x = x0; x < x1 && ok; ++x, ++it) {
                     if (mine == 0 && x == max(x0, x1 - 4) && b < b_last) {
@@ -346,17 +351,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int nb = S.of_tile(x1);          // the next entry with tiles here
                         const Entry ne = entry_of<kPaged>(nb, p);
                         tma_prefetch_l2_4d(&tmQn, 0, ne.row0, chunk0, ne.seq);
-                        if (rank == 1) {
-                            tma_prefetch_l2_3d(&tmQp, 0, ne.row0, ne.seq);
-                            tma_prefetch_l2_3d(&tmQp, 0, ne.row0 + 64, ne.seq);
-                        }
+                        tma_prefetch_l2_3d(&tmQp, rope0, ne.row0, ne.seq);
+                        tma_prefetch_l2_3d(&tmQp, rope0, ne.row0 + 64, ne.seq);
                         const long long nn = min(S.start(nb + 1), t_end) - x1;
                         for (int j = 0; j < min(nn, 3LL); ++j) {
                             const int r = kPaged ? 0 : j * kBN;
                             const int o = kPaged ? __ldg(p.block_table + static_cast<size_t>(ne.seq) * p.max_pages + j)
                                                  : ne.seq;
                             tma_prefetch_l2_4d(&tmKV, 0, r, chunk0, o);
-                            if (rank == 1) tma_prefetch_l2_3d(&tmKp, 0, r, o);
+                            tma_prefetch_l2_3d(&tmKp, rope0, r, o);
                         }
                     }
                     const int tile = static_cast<int>(x - P0);          // tile of the sequence
@@ -372,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], kvbytes);
                     tma_load_4d(dst, &tmKV, &c.full[s], 0, row0, chunk0, outer);   // 4 latent chunks
-                    if (rank == 1) tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], 0, row0, outer);
+                    tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], rope0, row0, outer);   // RoPE half
                 }
                 if (!ok) break;
             }
@@ -456,10 +459,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_fence_after_sync();
                         // S_part = Q_part K_part^T: Q from TMEM (8 columns per 16 dims).
                         const uint64_t kvd = smem_desc_sw128(sKVa + s_stage * kStageBytes, 16, 1024);
-                        if (rank == 0)
-                            issue_s<16>(tbase + kColS, tbase + kColQ, kvd, idS);
-                        else
-                            issue_s<20>(tbase + kColS, tbase + kColQ, kvd, idS);
+                        const uint64_t rpd = smem_desc_sw64_kmajor(sKVa + s_stage * kStageBytes + 4 * kKvChunk);
+                        issue_s(tbase + kColS, tbase + kColQ, kvd, rpd, idS);
                         umma_commit(&c.s_full);
                         ++gs;
                         ++s_x;
@@ -526,18 +527,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     tmem_st_x32(tbase + lane_base + kColQ + (2 * qi + j) * 32, r);
                 }
-                if (rank == 1 && (row >> 6) == qi) {   // warp-uniform: heads [64 qi, 64 qi + 64) of Q_pe
-                    const uint4 *rowp = reinterpret_cast<const uint4 *>(src + 2 * kQChunk + (row & 63) * 128);
-                    uint32_t r[32];
+                if ((row >> 6) == qi) {   // warp-uniform: heads [64 qi, 64 qi + 64) of this CTA's Q_pe half
+                    // 64-byte rows, 64-byte swizzle: 16-byte piece k of row rr sits at k ^ ((rr >> 1) & 3)
+                    const int rr = row & 63;
+                    const uint4 *rowp = reinterpret_cast<const uint4 *>(src + 2 * kQChunk + rr * 64);
+                    uint32_t r[16];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint4 v = rowp[k ^ swz];
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = rowp[k ^ ((rr >> 1) & 3)];
                         r[4 * k] = v.x;
                         r[4 * k + 1] = v.y;
                         r[4 * k + 2] = v.z;
                         r[4 * k + 3] = v.w;
                     }
-                    tmem_st_x32(tbase + lane_base + kColQ + 128, r);
+                    tmem_st_x16(tbase + lane_base + kColQ + 128, r);
                 }
                 named_barrier(kBarX, 128);          // every row read: the slot goes back to the producer
                 if (leader) mbar_arrive(&c.empty[st]);
@@ -1096,9 +1099,9 @@ int launch_mla_decode(const void *Q_nope, const void *Q_pe, const void *KV_laten
     }
     CUtensorMap tkv, tkp, tqn, tqp;
     if (!make_tma_bf16_chunked(tkv, KV_latent, d_c, N_kv, B, kBN, 4, err) ||
-        !make_tma_bf16_3d(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
+        !make_tma_bf16_3d_sw64(tkp, K_pe, d_r, N_kv, B, kBN, err) ||
         !make_tma_bf16_chunked(tqn, Q_nope, d_c, H, B, kH, 2, err) ||
-        !make_tma_bf16_3d(tqp, Q_pe, d_r, H, B, kH / 2, err))
+        !make_tma_bf16_3d_sw64(tqp, Q_pe, d_r, H, B, kH / 2, err))
         return 5;
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
@@ -1189,9 +1192,9 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
     }
     CUtensorMap tkv, tkp, tqn, tqp;
     if (!make_tma_bf16_chunked(tkv, KV_cache, d_c, kBN, num_pages, kBN, 4, err) ||
-        !make_tma_bf16_3d(tkp, K_pe_cache, d_r, kBN, num_pages, kBN, err) ||
+        !make_tma_bf16_3d_sw64(tkp, K_pe_cache, d_r, kBN, num_pages, kBN, err) ||
         !make_tma_bf16_chunked(tqn, Q_nope, d_c, static_cast<uint64_t>(s_q) * H, B_seq, kH, 2, err) ||
-        !make_tma_bf16_3d(tqp, Q_pe, d_r, static_cast<uint64_t>(s_q) * H, B_seq, kH / 2, err))
+        !make_tma_bf16_3d_sw64(tqp, Q_pe, d_r, static_cast<uint64_t>(s_q) * H, B_seq, kH / 2, err))
         return 5;
     const size_t slots = static_cast<size_t>(C) * 2;
     Params p;

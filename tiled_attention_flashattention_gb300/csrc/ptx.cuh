@@ -300,6 +300,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Shared-memory matrix descriptor for a 64-byte-swizzled K-major operand
+// (rows of 32 bf16 along K, 8-row groups 512 bytes apart, every swizzle atom
+// 512-byte aligned): layout type 4 in bits 61-63; step K by 16 elements by
+// adding 32 bytes to start.
+__device__ __forceinline__ uint64_t smem_desc_sw64_kmajor(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((16u >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
+    return d;
+}
+
 // Descriptor of the same operand shifted by byte_off bytes (a multiple of 16):
 // only the start-address field changes.  Shared memory is below 256 KB, so the
 // 14-bit field never carries into the next one.
