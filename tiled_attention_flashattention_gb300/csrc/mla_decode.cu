@@ -23,7 +23,7 @@
 // online softmax; each then multiplies P by its own latent half
 // (V = KV_latent).  Send and receive buffers, and P in TMEM, are
 // double-buffered, so the copy of one unit overlaps the softmax of the other
-// and the tensor cores never wait for the exchange round trip.
+// and the next tile's S overlaps both.
 //
 // Work split: the B * ceil(N_kv / 64) key tiles are cut into one contiguous
 // range per cluster (as many clusters as fit on the GPU at once).  A range
@@ -37,8 +37,9 @@
 // workspace holds two slots per cluster whatever B and N_kv are.
 //
 // Per CTA (384 threads, one CTA per SM):
-//   warp 0      TMA producer: through one ring of 4 stages, each range's query
-//               part (two slots) and then this CTA's dims of its 64-key tiles;
+//   warps 0, 2  TMA producers (each owns alternate stages of one 4-stage ring):
+//               each range's query part (two slots), then this CTA's dims of
+//               its 64-key tiles;
 //   warp 1      tcgen05 issuer: S_part = Q_part K_part^T per tile (Q from
 //               TMEM, N = 64) and O_half += P V_half per unit (P from TMEM,
 //               N = 256), each issued as soon as its inputs are ready;
