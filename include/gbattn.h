@@ -319,6 +319,31 @@ int gbattn_set_fault_injection(int mode);
 int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void *V,
                          float *S, float *O, void *stream);
 
+/*
+ * gbattn_mla_trace -- latency trace of the MLA decode kernel (observability; the
+ * pages have no counterpart).  Only a library built with -DGBATTN_TRACE (the
+ * package's trace build) records it; the default library returns
+ * GBATTN_ERR_UNSUPPORTED and writes nothing.
+ *
+ * In the trace build every launch of the MLA split kernel stamps, for the
+ * first GBATTN_MLA_TRACE_TILES key tiles of cluster 20 (cluster 0 when fewer
+ * than 21 clusters run), the device global timer (ns) at each step of a tile's
+ * chain, for both CTAs of the cluster.  This call synchronises the device,
+ * copies the stamps of the launches since the last call to `host` and clears
+ * them.  Layout: uint64 [2 CTAs][GBATTN_MLA_TRACE_EVENTS][GBATTN_MLA_TRACE_TILES],
+ * 0 = not reached; a later launch overwrites the stamps it reaches.  Events, in
+ * order: load issued, S MMA issued, P V issued for unit 0 and unit 1, S read
+ * from tensor memory, send buffer 0 / 1 free, copy 0 / 1 issued to the peer,
+ * softmax has unit 0 / 1 (both partials), P of unit 0 / 1 written.
+ *   host: caller-owned, at least GBATTN_MLA_TRACE_BYTES bytes.
+ * Errors: GBATTN_ERR_UNSUPPORTED (default library), GBATTN_ERR_INVALID_ARG
+ * (host NULL or bytes too small), GBATTN_ERR_LAUNCH.
+ */
+#define GBATTN_MLA_TRACE_EVENTS 13
+#define GBATTN_MLA_TRACE_TILES 64
+#define GBATTN_MLA_TRACE_BYTES (8 * 2 * GBATTN_MLA_TRACE_EVENTS * GBATTN_MLA_TRACE_TILES)
+int gbattn_mla_trace(void *host, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

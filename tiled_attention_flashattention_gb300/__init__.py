@@ -19,12 +19,14 @@ import torch
 __all__ = ["attn_fwd", "attn_fwd_sparse", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_paged",
            "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan", "attn_fwd_host",
            "attn_fwd_host_device_bytes", "mla_decode_host", "mla_decode_host_device_bytes",
-           "check", "selftest_umma",
+           "check", "selftest_umma", "mla_trace", "MLA_TRACE_EVENTS",
            "set_wait_timeout_ns", "set_fault_injection", "GbattnError", "library_path", "load_library"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+_LIB_TRACE_PATH = os.path.join(_PKG, "libgbattn_trace.so")
 _lib = None
+_lib_trace = False
 _lock = threading.Lock()
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "WORKSPACE", 5: "LAUNCH",
@@ -41,16 +43,23 @@ def library_path() -> str:
     return _LIB_PATH
 
 
-def load_library():
-    """Load libgbattn.so (built by ``__graft_entry__.build()``); raise if it is missing."""
-    global _lib
+def load_library(trace: bool = False):
+    """Load libgbattn.so (built by ``__graft_entry__.build()``), or with
+    trace=True the trace build libgbattn_trace.so (``_build.build(trace=True)``);
+    one of the two per process.  Raise if it is missing."""
+    global _lib, _lib_trace
     with _lock:
         if _lib is not None:
+            if trace and not _lib_trace:
+                raise RuntimeError("the default library is already loaded in this process; "
+                                   "load the trace build first, in a process of its own")
             return _lib
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError(f"{_LIB_PATH} is missing: build it first "
-                               "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(_LIB_PATH)
+        path = _LIB_TRACE_PATH if trace else _LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()'" +
+                               (", then _build.build(trace=True))" if trace else ")"))
+        lib = ctypes.CDLL(path)
         P, I, F, SZ, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd.restype = I
@@ -86,7 +95,10 @@ def load_library():
         lib.gbattn_set_fault_injection.restype = I
         lib.gbattn_selftest_umma.argtypes = [P, P, P, P, P, P, P]
         lib.gbattn_selftest_umma.restype = I
+        lib.gbattn_mla_trace.argtypes = [P, SZ]
+        lib.gbattn_mla_trace.restype = I
         _lib = lib
+        _lib_trace = trace
         return lib
 
 
@@ -437,3 +449,19 @@ def selftest_umma(A, B, P, V, stream=None):
                                   ctypes.c_void_p(_stream_handle(stream)))
     _raise_if(rc)
     return S, O
+
+
+# Layout of gbattn_mla_trace (include/gbattn.h): [2 CTAs][events][64 tiles] of
+# global-timer ns, 0 where a step was not reached.
+MLA_TRACE_EVENTS = ("load", "s_issue", "pv0_issue", "pv1_issue", "s_read", "send_buf0_free", "send_buf1_free",
+                    "copy0_issue", "copy1_issue", "softmax0_in", "softmax1_in", "p0_ready", "p1_ready")
+_MLA_TRACE_TILES = 64
+
+
+def mla_trace():
+    """Stamps of the MLA decode launches since the last call (trace build only:
+    ``load_library(trace=True)``), as a uint64 numpy array [2, 13, 64]; clears them."""
+    import numpy as np
+    buf = np.zeros((2, len(MLA_TRACE_EVENTS), _MLA_TRACE_TILES), dtype=np.uint64)
+    _raise_if(load_library().gbattn_mla_trace(ctypes.c_void_p(buf.ctypes.data), buf.nbytes))
+    return buf

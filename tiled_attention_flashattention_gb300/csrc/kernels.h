@@ -69,6 +69,10 @@ int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *
                               void *O, float *LSE, int B, int H, int N_kv, int d_c, int d_r, float scale,
                               const LaunchEnv &env, std::string &err);
 
+// MLA decode latency trace (gbattn_mla_trace): copies and clears the stamps of
+// the trace build; returns a gbattn_status value (UNSUPPORTED otherwise).
+int mla_trace_fetch(void *host, size_t bytes, std::string &err);
+
 // Mamba-2 SSD scan (ssd_scan).
 int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *Bm, const void *Cm, const float *D,
                     float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, const LaunchEnv &env,

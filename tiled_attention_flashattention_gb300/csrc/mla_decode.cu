@@ -56,6 +56,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "gbattn.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -65,6 +66,15 @@ namespace {
 constexpr int kH = 128;                   // heads per tile (MMA M)
 constexpr int kBN = 64;                   // keys per tile (TMA stage, S MMA N)
 constexpr int kBU = 32;                   // keys per unit (exchange, softmax, PV)
+// Trace build: events per tile, tiles per cluster and the cluster recorded.
+enum TraceEvent : int {
+    kTrLoad = 0, kTrSIssue, kTrPV0, kTrPV1, kTrSRead, kTrSendBuf0, kTrSendBuf1, kTrCopy0, kTrCopy1,
+    kTrSoftmax0, kTrSoftmax1, kTrP0, kTrP1, kTraceEvents
+};
+#ifdef GBATTN_TRACE
+constexpr int kTraceTiles = 64;
+constexpr int kTraceCluster = 20;
+#endif
 constexpr int kDc = 512;
 constexpr int kHalf = 256;                // latent dims owned by one CTA
 constexpr int kKvChunk = kBN * 128;       // [64 keys x 64 dims] bf16, one TMA box
@@ -236,6 +246,23 @@ __device__ __forceinline__ void issue_s(uint32_t d, uint32_t a, uint64_t kvd, ui
     for (int k = 16; k < kSSteps; ++k) umma_ts(d, a + k * 8, desc_advance(rpd, (k - 16) * 32), idesc, 1u);
 }
 
+// Event stamps for latency studies, compiled in only with -DGBATTN_TRACE (the
+// library's trace build): per tile of one cluster's range, the global timer (ns)
+// at each step of the tile's chain, [CTA rank][event][tile], 0 = not reached.
+// The events are listed with gbattn_mla_trace in the public header.
+#ifdef GBATTN_TRACE
+__device__ unsigned long long g_mla_trace[2][kTraceEvents][kTraceTiles];
+#define MLA_TRACE(e, i)                                                                         \
+    do {                                                                                        \
+        if (cl == (p.C > kTraceCluster ? kTraceCluster : 0) && (i) >= 0 && (i) < kTraceTiles)   \
+            g_mla_trace[rank][e][i] = global_timer_ns();                                        \
+    } while (0)
+#else
+#define MLA_TRACE(e, i) \
+    do {                \
+    } while (0)
+#endif
+
 template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_split_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKp,
@@ -375,6 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (round > 0 && !(ok = mbar_wait(&c.empty[s], (round & 1u) ^ 1u, ctl))) break;
                     uint8_t *dst = sKV + s * kStageBytes;
                     mbar_arrive_expect_tx(&c.full[s], kvbytes);
+                    MLA_TRACE(kTrLoad, static_cast<int>(x - t_begin));
                     tma_load_4d(dst, &tmKV, &c.full[s], 0, row0, chunk0, outer);   // 4 latent chunks
                     tma_load_3d(dst + 4 * kKvChunk, &tmKp, &c.full[s], rope0, row0, outer);   // RoPE half
                 }
@@ -435,6 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int k = 1; k < kBU / 16; ++k)
                             umma_ts(tbase + kColO, tp + k * 8, desc_advance(vd, k * 2048), idPV, 1u);
                         umma_commit(&c.pfree[h]);
+                        MLA_TRACE(kTrPV0 + h, gu >> 1);
                         if (h == 1) {
                             umma_commit(&c.empty[u_stage]);
                             ++u_slot;
@@ -463,6 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint64_t rpd = smem_desc_sw64_kmajor(sKVa + s_stage * kStageBytes + 4 * kKvChunk);
                         issue_s(tbase + kColS, tbase + kColQ, kvd, rpd, idS);
                         umma_commit(&c.s_full);
+                        MLA_TRACE(kTrSIssue, gs);
                         ++gs;
                         ++s_x;
                         if (s_x == s_bnd || gs == total) umma_commit(&c.q_empty);   // last tile of a range
@@ -564,6 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 uint32_t sr[kBN];
                 tmem_ld_x64(tbase + lane_base + kColS, sr);
+                if (leader) MLA_TRACE(kTrSRead, static_cast<int>(t));
                 tc_fence_before_sync();
                 mbar_arrive(&c.s_free);
                 if constexpr (kPaged) {
@@ -599,6 +630,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_wait_read_allow1();
                         got = mbar_wait(&c.own_free[h], (t - 1) & 1u, ctl);
                     }
+                    if (leader) MLA_TRACE(kTrSendBuf0 + h, static_cast<int>(t));
                     if (!(ok = barrier_and(kBarX, 128, got))) break;
                     float4 *srow = reinterpret_cast<float4 *>(sSend + h * kXBytes + row * 128);
 #pragma unroll
@@ -614,6 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             mbar_arrive_expect_tx(&c.xfull[h], kXBytes);   // the peer's unit (t, h)
                             bulk_copy_to_peer(peer_recv[h], sSend + h * kXBytes, kXBytes, peer_xfull[h]);
                             bulk_commit_group();
+                            MLA_TRACE(kTrCopy0 + h, static_cast<int>(t));
                             mbar_arrive(&c.sent[h]);
                         }
                     }
@@ -673,6 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // all 128 rows read: the sender may reuse send buffer h and the
                     // peer may copy its next unit into receive buffer h
                     if (!(ok = barrier_and(kBarS, 128, got && okw))) break;
+                    if (leader) MLA_TRACE(kTrSoftmax0 + h, static_cast<int>(t));
                     if (leader) {
                         mbar_arrive(&c.own_free[h]);
                         mbar_arrive_remote(peer_xfree[h]);
@@ -723,6 +757,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_st_x16(tbase + lane_base + kColP + h * (kBU / 2), pk);
                     tmem_st_wait();
                     tc_fence_before_sync();
+                    if (leader) MLA_TRACE(kTrP0 + h, static_cast<int>(t));
                     mbar_arrive(&c.p_full[h]);
                 }
             }
@@ -1259,6 +1294,35 @@ int launch_mla_decode_paged(const void *Q_nope, const void *Q_pe, const void *KV
         return 5;
     }
     return 0;
+}
+
+int mla_trace_fetch(void *host, size_t bytes, std::string &err)
+{
+#ifdef GBATTN_TRACE
+    static_assert(kTraceEvents == GBATTN_MLA_TRACE_EVENTS && kTraceTiles == GBATTN_MLA_TRACE_TILES,
+                  "trace layout of the public header");
+    constexpr size_t need = sizeof(g_mla_trace);
+    if (host == nullptr || bytes < need) {
+        err = "gbattn_mla_trace: host buffer missing or smaller than GBATTN_MLA_TRACE_BYTES";
+        return GBATTN_ERR_INVALID_ARG;
+    }
+    void *dev = nullptr;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(host, g_mla_trace, need);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&dev, g_mla_trace);
+    if (e == cudaSuccess) e = cudaMemset(dev, 0, need);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        err = std::string("gbattn_mla_trace: ") + cudaGetErrorString(e);
+        return GBATTN_ERR_LAUNCH;
+    }
+    return GBATTN_OK;
+#else
+    (void)host;
+    (void)bytes;
+    err = "gbattn_mla_trace: this library was built without GBATTN_TRACE";
+    return GBATTN_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // namespace gbattn
