@@ -1,8 +1,8 @@
 """GPU parity of attn_fwd_sparse (block-sparse mask of 128 x 128 blocks,
 through the C ABI) against the fp64 oracle: random masks with and without
 causal / window, one query tile of a CTA masked out while the other is not,
-empty masks, bit-equality with attn_fwd for an all-ones mask, determinism and
-a sampled long causal GQA case."""
+empty masks, an all-ones mask against attn_fwd, determinism and a sampled long
+causal GQA case."""
 import numpy as np
 import pytest
 import torch
@@ -65,13 +65,21 @@ def test_one_query_tile_of_a_cta_masked_out():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_all_ones_mask_is_attn_fwd_bitwise(causal):
+def test_all_ones_mask_is_attn_fwd(causal):
+    # An all-ones mask removes nothing: the block-sparse kernel (128-key tiles)
+    # computes the dense attention.  attn_fwd runs these short rows in its
+    # pipelined 64-key form, so the two round differently: each is held to the
+    # oracle, and to the other within twice the bar.
     Q, K, V = wl.random_prefill(2, 4, 2, 777, 777, 128, seed=61)
     mask = torch.ones(2, 4, 7, 7, dtype=torch.uint8)
     O1, L1 = gb.attn_fwd(Q.cuda(), K.cuda(), V.cuda(), causal=causal, scale=0.1)
+    gb.check()
     O2, L2 = run(Q, K, V, mask, causal, 0, 0.1)
-    assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
-    assert torch.equal(L1, L2)
+    O_ref, L_ref = oracle.attn_fwd(Q, K, V, causal, 0, 0.1)
+    compare(O1, L1, O_ref, L_ref, what="dense")
+    compare(O2, L2, O_ref, L_ref, what="all-ones mask")
+    compare(O2, L2, O1.float().cpu().double().numpy(), L1.cpu().double().numpy(), o_tol=4e-2, lse_tol=2e-3,
+            what="all-ones mask against dense")
 
 
 def test_deterministic():

@@ -19,13 +19,17 @@
 // The two Q tiles ping-pong: while the softmax warps work on tile 0's scores,
 // the tensor core computes tile 1's scores and PV products, and vice versa
 // (FlashAttention-2's point about keeping non-matmul work off the critical
-// path, TileLang 学习笔记 "FlashAttention-2 的改进").  The one-Q-tile form
-// (256 threads, warps 0-7) runs two CTAs per SM instead, and the other CTA
-// fills the tensor core while one CTA's softmax works (see Cfg).
+// path, TileLang 学习笔记 "FlashAttention-2 的改进").  The one-Q-tile forms
+// (256 threads, warps 0-7) run two CTAs per SM instead, so the other CTA fills
+// the tensor core while one CTA's softmax works; the dense one ("pipelined")
+// works on 64-key tiles with two S buffers, issuing the score MMA of key tile
+// j + 1 before the P V of tile j, so within the CTA too the next scores are
+// computed while the softmax works on the current ones (see Cfg).
 //
-// TMEM (32-bit columns x 128 lanes): S_t at 128 t and O_t after the kT S
-// tiles (two-tile form: S0 [0,128), S1 [128,256), O0 [256, 256+D),
-// O1 [256+D, 256+2D)).  P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+// TMEM (32-bit columns x 128 lanes): two-tile form S0 [0,128), S1 [128,256),
+// O0 [256, 256+D), O1 [256+D, 256+2D); block-sparse one-tile form S [0,128),
+// O [128, 128+D); pipelined form S buffers [0,64), [64,128), O [128, 128+D).
+// P (bf16 pairs) overwrites the first half of its S.
 //
 // The running maximum is updated lazily: the reference maximum m_ref moves
 // only when a new score exceeds it by more than 8 in log2 units.  Until then
@@ -42,36 +46,49 @@ namespace gbattn {
 namespace {
 
 constexpr int kBM = 128;       // query rows per Q tile
-constexpr int kBN = 128;       // keys per K/V tile
-constexpr int kChunkBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B)
+constexpr int kBN = 128;       // keys per K/V tile of the two-tile and block-sparse forms (and of the mask)
+constexpr int kQChunkBytes = kBM * 128;  // one TMA box of a Q (or O) tile: 128 rows x 64 bf16 (128 B)
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.693147180559945309f;
 
-// Two forms, by the number kT of 128-row Q tiles per CTA:
-//   kT = 2: one CTA per SM, 384 threads (two softmax warpgroups ping-pong on
-//           the tensor core), 512 TMEM columns, a ring of 5 (d=128) / 10
-//           (d=64) K/V slots;
+// Forms, by the number kT of 128-row Q tiles per CTA and the key tile BN:
+//   kT = 2, BN = 128: one CTA per SM, 384 threads (two softmax warpgroups
+//           ping-pong on the tensor core), 512 TMEM columns, a ring of 5
+//           (d=128) / 10 (d=64) K/V slots;
 //   kT = 1: two CTAs per SM, 256 threads (one softmax warpgroup; the other
-//           CTA fills the tensor core while it works), 256 TMEM columns, a
-//           ring of 2 / 5 slots.  One CTA's start-up and drain overlap the
-//           other's main loop, and the finer work items balance better.
+//           CTA fills the tensor core while it works), 256 TMEM columns.  One
+//           CTA's start-up and drain overlap the other's main loop, and the
+//           finer work items balance better.  BN = 64 (dense, pipelined): two
+//           S buffers, a ring of 4 / 10 slots of 64-key K or V tiles loaded in
+//           the issuer's order (K of tile j + 1 before V of tile j); BN = 128
+//           (block-sparse, whose mask is in 128-key blocks): one S, a ring of
+//           2 / 5 slots.
 // Registers per thread after the per-role split (setmaxnreg): warpgroup 0
 // (producer, MMA issuer, idle warps) gives registers to the softmax
 // warpgroups, which hold a 128-float score row per thread.  kT = 2:
 // 128 * 104 + 256 * 200 = 64,512 = 384 * 168; kT = 1: 128 * 64 + 128 * 192
 // (or 56 + 200 where that avoids spills) = 32,768 = 256 * 128, the registers
 // each block is launched with.
-template <int D, int kT>
+// BN keys per K/V tile: 128, or 64 for the pipelined one-tile form (kT = 1,
+// kPipe): its two 64-column S buffers let the score MMA of key tile j + 1 run
+// while the softmax works on tile j, inside one CTA, and two such CTAs still
+// fit an SM (256 TMEM columns, under 100 KB of shared memory each).
+template <int D, int kT, int BN = kBN>
 struct Cfg {
+    static constexpr bool kPipe = kT == 1 && BN == 64;
     static constexpr int kChunks = D / 64;
-    static constexpr int kTileBytes = kBM * D * 2;
-    static constexpr int kSlots = kT == 2 ? ((D == 128) ? 5 : 10) : ((D == 128) ? 2 : 5);
+    static constexpr int kQTileBytes = kBM * D * 2;
+    static constexpr int kKvTileBytes = BN * D * 2;
+    static constexpr int kKvChunkBytes = BN * 128;   // one TMA box of a K/V tile: BN rows x 64 bf16
+    static constexpr int kSlots = kT == 2 ? ((D == 128) ? 5 : 10)
+                                          : (kPipe ? ((D == 128) ? 4 : 10) : ((D == 128) ? 2 : 5));
     static constexpr uint32_t kTmemCols = kT == 2 ? 512 : 256;
     static constexpr int kThreads = kT == 2 ? 384 : 256;
     static constexpr int kMinBlocks = kT == 2 ? 1 : 2;
-    // TMEM columns of S_t (P_t overwrites its first 64) and O_t.
-    __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-    __host__ __device__ static constexpr uint32_t col_o(int t) { return 128u * kT + D * t; }
+    // TMEM columns of S buffer i (P overwrites its first BN / 2) and of O_t:
+    // two-tile form S_t of Q tile t at 128 t; pipelined form S buffers at 0, 64.
+    __host__ __device__ static constexpr uint32_t col_s(int i) { return static_cast<uint32_t>(BN) * i; }
+    __host__ __device__ static constexpr uint32_t col_o(int t) { return (kPipe ? 128u : 128u * kT) + D * t; }
 };
 
 struct Ctl {
@@ -81,16 +98,19 @@ struct Ctl {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_final[2];
+    uint64_t pv_done;       // pipelined form: P V of a key tile complete (O stable for a rescale)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int sp_lo[2], sp_hi[2];     // block-sparse form: first / last + 1 active key block of each Q tile
 };
 
-template <int D, int kT>
+template <int D, int kT, int BN>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(kT + Cfg<D, kT>::kSlots) * Cfg<D, kT>::kTileBytes + sizeof(Ctl);
+    using C = Cfg<D, kT, BN>;
+    return 1024 + static_cast<size_t>(kT) * C::kQTileBytes + static_cast<size_t>(C::kSlots) * C::kKvTileBytes +
+           sizeof(Ctl);
 }
 
 struct Params {
@@ -116,34 +136,39 @@ struct Range {
     int lo, hi;         // KV tiles [lo, hi); empty when lo >= hi
 };
 
-// KV tiles touched by query rows [r0, r1) (r1 > r0).
+// BN-key tiles touched by query rows [r0, r1) (r1 > r0).
+template <int BN>
 __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
 {
     const long long off = static_cast<long long>(p.N_kv) - p.N_q;
     const long long key_lo = max(0LL, r0 + off - p.lo_pad);                                   // inclusive
     const long long key_hi = min(static_cast<long long>(p.N_kv), r1 - 1 + off + p.hi_pad + 1);  // exclusive
     if (key_hi <= key_lo) return {0, 0};
-    return {static_cast<int>(key_lo / kBN), static_cast<int>((key_hi + kBN - 1) / kBN)};
+    return {static_cast<int>(key_lo / BN), static_cast<int>((key_hi + BN - 1) / BN)};
 }
 
-template <int D, bool kSparse, int kT>
-__global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
+template <int D, bool kSparse, int kT, int BN>
+__global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMinBlocks)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const Params p)
 {
-    using C = Cfg<D, kT>;
+    using C = Cfg<D, kT, BN>;
+    constexpr bool kPipe = C::kPipe;
+    static_assert(!kSparse || BN == kBN, "the block mask is in 128-key blocks");
+    static_assert(kT == 1 || BN == kBN, "the two-tile form uses 128-key tiles");
     constexpr bool kWideSoftmax = kT == 2 || (kSparse && D == 128);
-    constexpr uint32_t kRegsLow = kT == 2 ? 104 : (kWideSoftmax ? 56 : 64);
-    constexpr uint32_t kRegsHigh = kWideSoftmax ? 200 : 192;
+    // (the pipelined form's softmax holds a 64-float row: more go to the issuer)
+    constexpr uint32_t kRegsLow = kT == 2 ? 104 : (kWideSoftmax ? 56 : (C::kPipe ? 80 : 64));
+    constexpr uint32_t kRegsHigh = kWideSoftmax ? 200 : (C::kPipe ? 176 : 192);
     static_assert(kT == 2 ? 128 * kRegsLow + 256 * kRegsHigh <= 384 * 168
                           : 128 * kRegsLow + 128 * kRegsHigh == 256 * 128, "register split");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem;                                    // [kT][TileBytes]
-    uint8_t *ring = smem + kT * C::kTileBytes;             // [Slots][TileBytes]
-    Ctl &c = *reinterpret_cast<Ctl *>(ring + C::kSlots * C::kTileBytes);
+    uint8_t *sQ = smem;                                    // [kT][QTileBytes]
+    uint8_t *ring = smem + kT * C::kQTileBytes;            // [Slots][KvTileBytes]
+    Ctl &c = *reinterpret_cast<Ctl *>(ring + C::kSlots * C::kKvTileBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -162,7 +187,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
     for (int t = 0; t < 2; ++t) {
         r0[t] = t < kT ? qb * (kT * kBM) + t * kBM : p.N_q;     // kT = 1: tile 1 is absent
         r1[t] = min(r0[t] + kBM, p.N_q);
-        rng[t] = (r0[t] < p.N_q) ? kv_range(r0[t], r1[t], p) : Range{0, 0};
+        rng[t] = (r0[t] < p.N_q) ? kv_range<BN>(r0[t], r1[t], p) : Range{0, 0};
         has[t] = rng[t].lo < rng[t].hi;
         if (has[t]) {
             lo = min(lo, rng[t].lo);
@@ -206,6 +231,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             mbar_init(&c.p_full[t], 4 * 32);
             mbar_init(&c.o_final[t], 1);
         }
+        mbar_init(&c.pv_done, 1);
         mbar_init(&c.drain, 1);
         c.abort = 0;
         fence_mbar_init();
@@ -257,29 +283,57 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             tma_prefetch_desc(&tmV);
             uint32_t qbytes = 0;
             for (int t = 0; t < 2; ++t)
-                if (has[t]) qbytes += C::kTileBytes;
+                if (has[t]) qbytes += C::kQTileBytes;
             if (p.inject == 1) qbytes = 0;   // nothing ever completes q_full
             if (qbytes) {
                 mbar_arrive_expect_tx(&c.q_full, qbytes);
                 for (int t = 0; t < 2; ++t)
                     if (has[t])
                         for (int ch = 0; ch < C::kChunks; ++ch)
-                            tma_load_3d(sQ + t * C::kTileBytes + ch * kChunkBytes, &tmQ, &c.q_full,
+                            tma_load_3d(sQ + t * C::kQTileBytes + ch * kQChunkBytes, &tmQ, &c.q_full,
                                         ch * 64, r0[t], bh);
             }
             bool ok = true;
             int it = 0;
-            for (int j = first; j < hi && ok; j = next_any(j)) {
-                for (int kv = 0; kv < 2; ++kv) {
+            if constexpr (kPipe) {
+                // The issuer's order: K of tile 0, then for each tile n the K of
+                // tile n + 1 (its S runs first) and the V of tile n; the last
+                // tile has no next K.
+                const int ntile = hi - first;
+                for (int q = 0; q < 2 * ntile && ok; ++q) {
+                    int kv, n;
+                    if (q == 0) {
+                        kv = 0, n = 0;
+                    } else if (q == 2 * ntile - 1) {
+                        kv = 1, n = ntile - 1;
+                    } else if (q & 1) {
+                        kv = 0, n = (q + 1) / 2;
+                    } else {
+                        kv = 1, n = q / 2 - 1;
+                    }
                     const int slot = it % C::kSlots;
                     const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[slot], (round & 1u) ^ 1u, ctl))) break;
-                    mbar_arrive_expect_tx(&c.full[slot], C::kTileBytes);
+                    mbar_arrive_expect_tx(&c.full[slot], C::kKvTileBytes);
                     const CUtensorMap *m = kv ? &tmV : &tmK;
                     for (int ch = 0; ch < C::kChunks; ++ch)
-                        tma_load_3d(ring + slot * C::kTileBytes + ch * kChunkBytes, m, &c.full[slot],
-                                    ch * 64, j * kBN, kvh);
+                        tma_load_3d(ring + slot * C::kKvTileBytes + ch * C::kKvChunkBytes, m, &c.full[slot],
+                                    ch * 64, (first + n) * BN, kvh);
                     ++it;
+                }
+            } else {
+                for (int j = first; j < hi && ok; j = next_any(j)) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int slot = it % C::kSlots;
+                        const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
+                        if (round > 0 && !(ok = mbar_wait(&c.empty[slot], (round & 1u) ^ 1u, ctl))) break;
+                        mbar_arrive_expect_tx(&c.full[slot], C::kKvTileBytes);
+                        const CUtensorMap *m = kv ? &tmV : &tmK;
+                        for (int ch = 0; ch < C::kChunks; ++ch)
+                            tma_load_3d(ring + slot * C::kKvTileBytes + ch * C::kKvChunkBytes, m, &c.full[slot],
+                                        ch * 64, j * BN, kvh);
+                        ++it;
+                    }
                 }
             }
             if (!ok) {
@@ -295,38 +349,76 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
         // =================== tensor-core issuer ===================
         regs_dec<kRegsLow>();
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
+            constexpr uint32_t idS = idesc_bf16_f32(kBM, BN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
             const uint32_t sQa = smem_u32(sQ), ringa = smem_u32(ring);
             // S_t = Q_t K^T: K-major A and B, 16 bf16 (32 B) per MMA along d.
             const uint64_t qdesc[2] = {smem_desc_sw128(sQa, 16, 1024),
-                                       smem_desc_sw128(sQa + C::kTileBytes, 16, 1024)};
-            auto issue_S = [&](int t, int slot) {
+                                       smem_desc_sw128(sQa + C::kQTileBytes, 16, 1024)};
+            // S buffer sb = Q_t K^T (16 d per MMA; the 64-d chunks of Q and K are
+            // kQChunkBytes / kKvChunkBytes apart)
+            auto issue_S = [&](int t, int sb, int slot) {
                 const uint64_t ad = qdesc[t];
-                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes, 16, 1024);
-                umma_ss(tbase + C::col_s(t), ad, bd, idS, 0u);
+                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kKvTileBytes, 16, 1024);
+                umma_ss(tbase + C::col_s(sb), ad, bd, idS, 0u);
 #pragma unroll
                 for (int k = 1; k < D / 16; ++k) {
-                    const uint32_t koff = (k / 4) * kChunkBytes + (k % 4) * 32;
-                    umma_ss(tbase + C::col_s(t), desc_advance(ad, koff), desc_advance(bd, koff), idS, 1u);
+                    const uint32_t qoff = (k / 4) * kQChunkBytes + (k % 4) * 32;
+                    const uint32_t koff = (k / 4) * C::kKvChunkBytes + (k % 4) * 32;
+                    umma_ss(tbase + C::col_s(sb), desc_advance(ad, qoff), desc_advance(bd, koff), idS, 1u);
                 }
             };
             // O_t += P_t V: P from TMEM (8 columns per 16 keys), V N-major
             // (64-wide d chunks 16 KB apart, 16 keys = 2048 B per MMA).
             bool started[2] = {false, false};
-            auto issue_PV = [&](int t, int slot) {
-                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kTileBytes, kChunkBytes, 1024);
-                umma_ts(tbase + C::col_o(t), tbase + C::col_s(t), bd, idPV, started[t] ? 1u : 0u);
+            auto issue_PV = [&](int t, int sb, int slot) {
+                const uint64_t bd = smem_desc_sw128(ringa + slot * C::kKvTileBytes, C::kKvChunkBytes, 1024);
+                umma_ts(tbase + C::col_o(t), tbase + C::col_s(sb), bd, idPV, started[t] ? 1u : 0u);
 #pragma unroll
-                for (int k = 1; k < kBN / 16; ++k)
-                    umma_ts(tbase + C::col_o(t), tbase + C::col_s(t) + k * 8, desc_advance(bd, k * 2048), idPV, 1u);
+                for (int k = 1; k < BN / 16; ++k)
+                    umma_ts(tbase + C::col_o(t), tbase + C::col_s(sb) + k * 8, desc_advance(bd, k * 2048), idPV, 1u);
                 started[t] = true;
             };
             bool ok = true;
             int it = 0;
             uint32_t pcount[2] = {0, 0};
             if (first < hi) ok = mbar_wait(&c.q_full, 0, ctl);
-            if (ok && first < hi) {
+            if constexpr (kPipe) {
+                // One Q tile, key tiles n = 0 .. ntile - 1 (ring items 2n: K, 2n + 1: V).
+                // S of tile n + 1 goes to the other S buffer before P V of tile n,
+                // so it runs while the softmax works on tile n; that buffer's
+                // previous P was read by P V of tile n - 1, issued before it.
+                const int ntile = hi - first;
+                auto islot = [&](int i) { return i % C::kSlots; };
+                auto iphase = [&](int i) { return static_cast<uint32_t>(i / C::kSlots) & 1u; };
+                // ring items in the producer's order: K(0), then K(n + 1), V(n) per tile n
+                if (ok && ntile > 0 && (ok = mbar_wait(&c.full[islot(0)], iphase(0), ctl))) {
+                    tc_fence_after_sync();
+                    issue_S(0, 0, islot(0));
+                    umma_commit(&c.s_full[0]);
+                    umma_commit(&c.empty[islot(0)]);
+                }
+                it = 1;
+                for (int n = 0; n < ntile && ok; ++n) {
+                    if (n + 1 < ntile) {
+                        const int ik = it++;
+                        if (!(ok = mbar_wait(&c.full[islot(ik)], iphase(ik), ctl))) break;
+                        tc_fence_after_sync();
+                        issue_S(0, (n + 1) & 1, islot(ik));
+                        umma_commit(&c.s_full[(n + 1) & 1]);
+                        umma_commit(&c.empty[islot(ik)]);
+                    }
+                    const int iv = it++;
+                    if (!(ok = mbar_wait(&c.full[islot(iv)], iphase(iv), ctl))) break;
+                    // P of tile n: one barrier per S buffer (the softmax may already have
+                    // finished tile n + 1, whose S was issued above)
+                    if (!(ok = mbar_wait(&c.p_full[n & 1], static_cast<uint32_t>(n >> 1) & 1u, ctl))) break;
+                    tc_fence_after_sync();
+                    issue_PV(0, n & 1, islot(iv));
+                    umma_commit(&c.empty[islot(iv)]);
+                    umma_commit(&c.pv_done);
+                }
+            } else if (ok && first < hi) {
                 const int slotK = 0;
                 ok = mbar_wait(&c.full[slotK], 0, ctl);
                 ++it;
@@ -334,7 +426,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                     tc_fence_after_sync();
                     for (int t = 0; t < 2; ++t)
                         if (act(t, first)) {
-                            issue_S(t, slotK);
+                            issue_S(t, t, slotK);
                             umma_commit(&c.s_full[t]);
                         }
                     umma_commit(&c.empty[slotK]);
@@ -343,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             // Key blocks in the producer's order (every block some Q tile computes):
             // PV of block j for tile 0, S of the next block for tile 0, PV of j for
             // tile 1, S of the next block for tile 1.
-            for (int j = first; j < hi && ok;) {
+            for (int j = first; j < hi && ok && !kPipe;) {
                 const int slotV = it % C::kSlots;
                 if (!(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                     break;
@@ -351,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                 if (act(0, j)) {
                     if (!(ok = mbar_wait(&c.p_full[0], pcount[0]++ & 1u, ctl))) break;
                     tc_fence_after_sync();
-                    issue_PV(0, slotV);
+                    issue_PV(0, 0, slotV);
                 }
                 const int jn = next_any(j);
                 int slotK = -1;
@@ -361,19 +453,19 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                         break;
                     ++it;
                     if (act(0, jn)) {
-                        issue_S(0, slotK);
+                        issue_S(0, 0, slotK);
                         umma_commit(&c.s_full[0]);
                     }
                 }
                 if (act(1, j)) {
                     if (!(ok = mbar_wait(&c.p_full[1], pcount[1]++ & 1u, ctl))) break;
                     tc_fence_after_sync();
-                    issue_PV(1, slotV);
+                    issue_PV(1, 1, slotV);
                 }
                 umma_commit(&c.empty[slotV]);
                 if (slotK >= 0) {
                     if (act(1, jn)) {
-                        issue_S(1, slotK);
+                        issue_S(1, 1, slotK);
                         umma_commit(&c.s_full[1]);
                     }
                     umma_commit(&c.empty[slotK]);
@@ -398,7 +490,6 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
         const int row = r0[t] + quad * 32 + lane;
         const bool row_valid = row < p.N_q && r0[t] < p.N_q;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tbase + lane_base + C::col_s(t);
         const uint32_t tO = tbase + lane_base + C::col_o(t);
         const float cexp = p.c;
         const float thr = kRescaleLog2 / cexp;     // threshold in raw score units
@@ -417,35 +508,45 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                     continue;
                 }
             }
+            // S buffer and its phase: Q tile t's own (two-tile / one-tile form), or
+            // alternating between two (pipelined form; each buffer every other tile).
+            const int sb = kPipe ? (n & 1) : t;
+            const uint32_t sphase = static_cast<uint32_t>(kPipe ? (n >> 1) : n) & 1u;
+            const uint32_t tS = tbase + lane_base + C::col_s(sb);
             // tcgen05.ld/st below are warp-collective: keep the outcome warp-uniform.
-            ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[t], static_cast<uint32_t>(n) & 1u, ctl));
+            ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[sb], sphase, ctl));
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t sr[128];
-            tmem_ld_4x32(tS, sr);
-            float s[128];
+            float s[BN];
+            {
+                uint32_t sr[BN];
+                if constexpr (BN == 128)
+                    tmem_ld_4x32(tS, sr);
+                else
+                    tmem_ld_x64(tS, sr);
 #pragma unroll
-            for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+                for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
+            }
 
-            const int k0 = j * kBN;
-            const bool need_mask = (k0 + kBN > p.N_kv) || (k0 + kBN - 1 > r0[t] + off + p.hi_pad) ||
+            const int k0 = j * BN;
+            const bool need_mask = (k0 + BN > p.N_kv) || (k0 + BN - 1 > r0[t] + off + p.hi_pad) ||
                                    (k0 < (r1[t] - 1) + off - p.lo_pad);
             if (need_mask) {
 #pragma unroll
-                for (int i = 0; i < 128; ++i) {
+                for (int i = 0; i < BN; ++i) {
                     const int key = k0 + i;
                     const bool allowed = key >= key_min && key <= key_max;
                     if (!allowed) s[i] = -INFINITY;
                 }
             }
             // Row maximum as four independent chains and a tree, not one
-            // 127-deep dependency chain.
+            // (BN - 1)-deep dependency chain.
             float m4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 m4[q] = s[q];
 #pragma unroll
-                for (int i = 4 + q; i < 128; i += 4) m4[q] = fmaxf(m4[q], s[i]);
+                for (int i = 4 + q; i < BN; i += 4) m4[q] = fmaxf(m4[q], s[i]);
             }
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 
@@ -456,7 +557,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
             float sum2[2] = {0.f, 0.f};                 // independent partial sums
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < BN / 32; ++q) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -469,9 +570,16 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             }
             l = l * alpha + (sum2[0] + sum2[1]);
             if (n > 0 && __any_sync(0xffffffffu, move)) {
-                // O_t already holds the PV products of earlier tiles (their
-                // completion is covered by this tile's S commit); rescale it
-                // before this tile's PV, which waits for p_full below.
+                // O_t already holds the PV products of earlier tiles; rescale it
+                // before this tile's PV, which waits for p_full below.  Their
+                // completion is covered by this tile's S commit, except in the
+                // pipelined form, where S of this tile was issued before P V of
+                // the previous one: wait for that one's commit.
+                if constexpr (kPipe) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&c.pv_done, static_cast<uint32_t>(n - 1) & 1u, ctl));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
@@ -483,7 +591,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             }
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&c.p_full[t]);
+            mbar_arrive(&c.p_full[sb]);
         }
 
         // ---- epilogue: O / l -> bf16, staged in this tile's Q buffer (free:
@@ -496,13 +604,13 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
             if (ok) {
                 tc_fence_after_sync();
                 const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-                uint8_t *stage = sQ + t * C::kTileBytes;
+                uint8_t *stage = sQ + t * C::kQTileBytes;
                 const int r = quad * 32 + lane;
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
                     tmem_ld_x32(tO + ch * 32, o);
-                    uint8_t *dst_row = stage + (ch / 2) * kChunkBytes + r * 128;
+                    uint8_t *dst_row = stage + (ch / 2) * kQChunkBytes + r * 128;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint4 v;
@@ -520,7 +628,7 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
                 named_barrier(1 + t, 128);
                 if (quad == 0 && lane == 0) {
                     for (int ch = 0; ch < C::kChunks; ++ch)
-                        tma_store_3d(&tmO, stage + ch * kChunkBytes, ch * 64, r0[t], bh);
+                        tma_store_3d(&tmO, stage + ch * kQChunkBytes, ch * 64, r0[t], bh);
                     bulk_commit_group();
                     bulk_wait_all();        // stores complete before the CTA retires
                 }
@@ -543,21 +651,21 @@ __global__ void __launch_bounds__(Cfg<D, kT>::kThreads, Cfg<D, kT>::kMinBlocks)
     }
 }
 
-template <int D, bool kSparse, int kT>
+template <int D, bool kSparse, int kT, int BN = kBN>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
            const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
     static std::atomic<uint64_t> configured{0};   // one bit per device
-    const size_t smem = smem_bytes<D, kT>();
+    const size_t smem = smem_bytes<D, kT, BN>();
     {
-        cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(attn_fwd_kernel<D, kSparse, kT>), smem,
-                                            configured);
+        cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(attn_fwd_kernel<D, kSparse, kT, BN>),
+                                            smem, configured);
         if (e != cudaSuccess) {
             err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return 5;
         }
     }
-    attn_fwd_kernel<D, kSparse, kT><<<grid, Cfg<D, kT>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
+    attn_fwd_kernel<D, kSparse, kT, BN><<<grid, Cfg<D, kT, BN>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
@@ -615,12 +723,6 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         }
         return 0;
     }
-    CUtensorMap tq, tk, tv, to;
-    if (!make_tma_bf16_3d(tq, Q, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
-        !make_tma_bf16_3d(to, O, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
-        !make_tma_bf16_3d(tk, K, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err) ||
-        !make_tma_bf16_3d(tv, V, d, N_kv, static_cast<uint64_t>(B) * H_kv, kBN, err))
-        return 5;
     Params p;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
@@ -644,7 +746,15 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
     // Q tiles per CTA (see Cfg).  Block-sparse launches use one: their density
     // is not known here, and sparse rows are short.
     const int kt = (!block_mask && mean_kv_tiles(N_q, N_kv, p.lo_pad, p.hi_pad) >= kTwoTileMinKvTiles) ? 2 : 1;
+    // The dense one-tile form runs pipelined, on 64-key tiles (see Cfg).
+    const int bn = (!block_mask && kt == 1) ? 64 : kBN;
     p.n_qblk = (N_q + kt * kBM - 1) / (kt * kBM);
+    CUtensorMap tq, tk, tv, to;
+    if (!make_tma_bf16_3d(tq, Q, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
+        !make_tma_bf16_3d(to, O, d, N_q, static_cast<uint64_t>(B) * H, kBM, err) ||
+        !make_tma_bf16_3d(tk, K, d, N_kv, static_cast<uint64_t>(B) * H_kv, bn, err) ||
+        !make_tma_bf16_3d(tv, V, d, N_kv, static_cast<uint64_t>(B) * H_kv, bn, err))
+        return 5;
     p.c = scale * 1.4426950408889634f;
     p.inject = env.inject;
     p.status = env.status;
@@ -659,8 +769,8 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         return d == 128 ? launch<128, true, 1>(tq, tk, tv, to, p, g, env, err)
                         : launch<64, true, 1>(tq, tk, tv, to, p, g, env, err);
     if (kt == 1)
-        return d == 128 ? launch<128, false, 1>(tq, tk, tv, to, p, g, env, err)
-                        : launch<64, false, 1>(tq, tk, tv, to, p, g, env, err);
+        return d == 128 ? launch<128, false, 1, 64>(tq, tk, tv, to, p, g, env, err)
+                        : launch<64, false, 1, 64>(tq, tk, tv, to, p, g, env, err);
     return d == 128 ? launch<128, false, 2>(tq, tk, tv, to, p, g, env, err)
                     : launch<64, false, 2>(tq, tk, tv, to, p, g, env, err);
 }
