@@ -57,6 +57,14 @@ SMALL = [
     (1, 2, 2, 700, 700, 128, True, 129),
     (1, 2, 2, 700, 700, 128, True, 256),
     (1, 2, 2, 650, 650, 128, True, 650),    # window = N: same as causal
+    # the one-tile form runs on 64-key tiles: windows and lengths at its tile edges
+    (1, 2, 2, 700, 700, 128, True, 63),
+    (1, 2, 2, 700, 700, 64, True, 64),
+    (1, 2, 2, 700, 700, 128, True, 65),
+    (1, 2, 1, 64, 64, 128, True, 0),
+    (1, 2, 2, 65, 65, 128, False, 0),
+    (1, 2, 2, 191, 191, 64, False, 0),
+    (1, 2, 2, 600, 600, 128, False, 63),    # symmetric
     (1, 1, 1, 1, 1, 128, False, 0),
     (1, 1, 1, 1, 1000, 64, True, 0),
     (3, 8, 8, 130, 1, 128, False, 0),
