@@ -532,11 +532,22 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             const bool need_mask = (k0 + BN > p.N_kv) || (k0 + BN - 1 > r0[t] + off + p.hi_pad) ||
                                    (k0 < (r1[t] - 1) + off - p.lo_pad);
             if (need_mask) {
+                if constexpr (kPipe) {
+                    // key k0 + i is visible iff 0 <= i - lo_i <= span: one unsigned
+                    // compare per element (a row without keys masks everything)
+                    const int span = key_max - key_min;
+                    const int lo_i = span < 0 ? (1 << 30) : key_min - k0;
+                    const uint32_t uspan = span < 0 ? 0u : static_cast<uint32_t>(span);
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int key = k0 + i;
-                    const bool allowed = key >= key_min && key <= key_max;
-                    if (!allowed) s[i] = -INFINITY;
+                    for (int i = 0; i < BN; ++i)
+                        if (static_cast<uint32_t>(i - lo_i) > uspan) s[i] = -INFINITY;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BN; ++i) {
+                        const int key = k0 + i;
+                        const bool allowed = key >= key_min && key <= key_max;
+                        if (!allowed) s[i] = -INFINITY;
+                    }
                 }
             }
             // Row maximum as four independent chains and a tree, not one
