@@ -384,10 +384,10 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             uint32_t pcount[2] = {0, 0};
             if (first < hi) ok = mbar_wait(&c.q_full, 0, ctl);
             if constexpr (kPipe) {
-                // One Q tile, key tiles n = 0 .. ntile - 1 (ring items 2n: K, 2n + 1: V).
-                // S of tile n + 1 goes to the other S buffer before P V of tile n,
-                // so it runs while the softmax works on tile n; that buffer's
-                // previous P was read by P V of tile n - 1, issued before it.
+                // One Q tile, key tiles n = 0 .. ntile - 1.  S of tile n + 1 goes to
+                // the other S buffer before P V of tile n, so it runs while the
+                // softmax works on tile n; that buffer's previous P was read by P V
+                // of tile n - 1, issued before it.
                 const int ntile = hi - first;
                 auto islot = [&](int i) { return i % C::kSlots; };
                 auto iphase = [&](int i) { return static_cast<uint32_t>(i / C::kSlots) & 1u; };
