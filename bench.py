@@ -75,16 +75,17 @@ def allowed_pairs(N_q: int, N_kv: int, causal: bool, window: int) -> int:
 
 def prefill_form(c: wl.PrefillCase) -> str:
     """Which instance of the prefill kernel the library launches for this
-    workload: the host picks two 128-row Q tiles per CTA when a query tile
-    visits at least 16 key tiles on average, else one (same rule as the
-    launcher)."""
+    workload: the host picks two 128-row Q tiles per CTA (128-key tiles) when
+    a query tile visits at least 16 128-key tiles on average, else one Q tile
+    on 64-key tiles, pipelined (same rule as the launcher)."""
     lo, hi = key_bounds(np.arange(c.N_q, dtype=np.int64), c.N_q, c.N_kv, c.causal, c.window)
     tiles = []
     for t0 in range(0, c.N_q, 128):
         klo, khi = lo[t0:t0 + 128].min(), hi[t0:t0 + 128].max() + 1
         tiles.append(max(0, -(-khi // 128) - klo // 128) if khi > klo else 0)
-    kt = 2 if np.mean(tiles) >= 16 else 1
-    return f"attn_fwd_kernel<{c.d}, dense, {kt} Q tile{'s' if kt == 2 else ''} per CTA>"
+    if np.mean(tiles) >= 16:
+        return f"attn_fwd_kernel<{c.d}, dense, 2 Q tiles per CTA, 128-key tiles>"
+    return f"attn_fwd_kernel<{c.d}, dense, 1 Q tile per CTA, 64-key tiles, pipelined>"
 
 
 def bench_config(pc, dc, world):
