@@ -551,35 +551,48 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                 }
             }
             // Row maximum as four independent chains and a tree, not one
-            // (BN - 1)-deep dependency chain.
+            // (BN - 1)-deep dependency chain; three-input max, two elements
+            // per instruction.
             float m4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 m4[q] = s[q];
+                int i = 4 + q;
 #pragma unroll
-                for (int i = 4 + q; i < BN; i += 4) m4[q] = fmaxf(m4[q], s[i]);
+                for (; i + 4 < BN; i += 8) m4[q] = max3(m4[q], s[i], s[i + 4]);
+                if (i < BN) m4[q] = fmaxf(m4[q], s[i]);
             }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
 
             const bool move = mx > m_ref + thr;
             const float new_ref = move ? mx : m_ref;
             const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
             m_ref = new_ref;
             const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-            float sum2[2] = {0.f, 0.f};                 // independent partial sums
+            // Exponentials a pair of keys at a time: one packed multiply-add
+            // for the two exponents, one packed add into the running sums (two
+            // independent pairs of partial sums).
+            const uint64_t c2 = f2_pack(cexp, cexp), nb2 = f2_pack(-base, -base);
+            uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
             for (int q = 0; q < BN / 32; ++q) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[q * 32 + 2 * i], cexp, -base));
-                    const float p1 = ex2_approx(fmaf(s[q * 32 + 2 * i + 1], cexp, -base));
-                    sum2[i & 1] += p0 + p1;
+                    float x0, x1;
+                    f2_unpack(fma_f2(f2_pack(s[q * 32 + 2 * i], s[q * 32 + 2 * i + 1]), c2, nb2), x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    sum2[i & 1] = add_f2(sum2[i & 1], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_x16(tS + q * 16, pk);
             }
-            l = l * alpha + (sum2[0] + sum2[1]);
+            {
+                float a0, a1;
+                f2_unpack(add_f2(sum2[0], sum2[1]), a0, a1);
+                l = l * alpha + (a0 + a1);
+            }
             if (n > 0 && __any_sync(0xffffffffu, move)) {
                 // O_t already holds the PV products of earlier tiles; rescale it
                 // before this tile's PV, which waits for p_full below.  Their

@@ -629,4 +629,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// Packed fp32 pairs (sm_100 and later): two floats in one 64-bit register
+// pair, operated on by one instruction per pair.  Each lane of fma_f2 /
+// add_f2 / max3 rounds exactly like its scalar counterpart (fmaf, +, fmaxf).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi), round to nearest
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// (a.lo + b.lo, a.hi + b.hi), round to nearest
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// max(a, b, c) in one instruction (three-input max, sm_100 and later)
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 }  // namespace gbattn
