@@ -435,11 +435,25 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             // Key blocks in the producer's order (every block some Q tile computes):
             // PV of block j for tile 0, S of the next block for tile 0, PV of j for
             // tile 1, S of the next block for tile 1.
+            // K / V tiles are usually in the ring long before they are used, but a
+            // wait on a phase that has already completed still costs the issuing
+            // thread ~170 cycles.  Their barriers are tested without blocking
+            // (mbar_poll) ahead of an MMA issue, so the test's latency hides behind
+            // it, and the wait is skipped when the tile has landed (not in the
+            // block-sparse form, whose issuer has no registers to spare; measured
+            // slower in the pipelined one-tile form).
+            bool v_seen = false;
+            auto ring_poll = [&](int i) {
+                return mbar_poll(smem_u32(&c.full[i % C::kSlots]), static_cast<uint32_t>(i / C::kSlots) & 1u);
+            };
             for (int j = first; j < hi && ok && !kPipe;) {
                 const int slotV = it % C::kSlots;
-                if (!(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
+                if (!v_seen && !(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                     break;
                 ++it;
+                // (item `it` is the next block's K when there is one; otherwise the
+                // test's result is not used)
+                const bool k_seen = !kSparse && ring_poll(it);
                 if (act(0, j)) {
                     if (!(ok = mbar_wait(&c.p_full[0], pcount[0]++ & 1u, ctl))) break;
                     tc_fence_after_sync();
@@ -447,11 +461,13 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                 }
                 const int jn = next_any(j);
                 int slotK = -1;
+                v_seen = false;
                 if (jn < hi) {
                     slotK = it % C::kSlots;
-                    if (!(ok = mbar_wait(&c.full[slotK], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
+                    if (!k_seen && !(ok = mbar_wait(&c.full[slotK], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                         break;
                     ++it;
+                    v_seen = !kSparse && ring_poll(it);
                     if (act(0, jn)) {
                         issue_S(0, 0, slotK);
                         umma_commit(&c.s_full[0]);
