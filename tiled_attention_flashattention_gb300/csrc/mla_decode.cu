@@ -689,8 +689,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < n && ok; ++i, ++t) {
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
-                    const bool got = mbar_wait(&c.sent[h], t & 1u, ctl) &&
-                                     mbar_wait(&c.xfull[h], t & 1u, ctl);
+                    // A wait costs the thread ~170 cycles even on a completed phase:
+                    // test the unit's three barriers (own partial sent, the peer's
+                    // copy landed, P buffer h free) together without blocking, and
+                    // wait only on those not yet complete.
+                    const bool sent_seen = mbar_poll(smem_u32(&c.sent[h]), t & 1u);
+                    const bool xfull_seen = mbar_poll(smem_u32(&c.xfull[h]), t & 1u);
+                    const bool pfree_seen = t == 0 || mbar_poll(smem_u32(&c.pfree[h]), (t - 1) & 1u);
+                    const bool got = (sent_seen || mbar_wait(&c.sent[h], t & 1u, ctl)) &&
+                                     (xfull_seen || mbar_wait(&c.xfull[h], t & 1u, ctl));
                     float s[kBU];
                     const float4 *orow = reinterpret_cast<const float4 *>(sSend + h * kXBytes + row * 128);
                     const float4 *rrow = reinterpret_cast<const float4 *>(sRecv + h * kXBytes + row * 128);
@@ -720,24 +727,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     float mx = s[0];
 #pragma unroll
-                    for (int k = 1; k < kBU; ++k) mx = fmaxf(mx, s[k]);
+                    for (int k = 1; k + 1 < kBU; k += 2) mx = max3(mx, s[k], s[k + 1]);
+                    mx = fmaxf(mx, s[kBU - 1]);
                     const bool move = mx > m_ref + thr;
                     const float new_ref = move ? mx : m_ref;
                     const float alpha = move ? ex2_approx((m_ref - new_ref) * cexp) : 1.0f;
                     m_ref = new_ref;
                     const float base = (m_ref == -INFINITY) ? 0.f : m_ref * cexp;
-                    float sum = 0.f;
+                    // exponents and sums a pair of keys at a time (packed fp32)
+                    const uint64_t c2 = f2_pack(cexp, cexp), nb2 = f2_pack(-base, -base);
+                    uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
                     uint32_t pk[kBU / 2];
 #pragma unroll
                     for (int k = 0; k < kBU / 2; ++k) {
-                        const float p0 = ex2_approx(fmaf(s[2 * k], cexp, -base));
-                        const float p1 = ex2_approx(fmaf(s[2 * k + 1], cexp, -base));
-                        sum += p0 + p1;
+                        float x0, x1;
+                        f2_unpack(fma_f2(f2_pack(s[2 * k], s[2 * k + 1]), c2, nb2), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        sum2[k & 1] = add_f2(sum2[k & 1], f2_pack(p0, p1));
                         pk[k] = pack_bf16x2(p0, p1);
                     }
-                    l = l * alpha + sum;
+                    {
+                        float a0, a1;
+                        f2_unpack(add_f2(sum2[0], sum2[1]), a0, a1);
+                        l = l * alpha + (a0 + a1);
+                    }
                     // P buffer h was read by the MMA of unit (t - 1, h).
-                    if (t > 0) okw = __all_sync(0xffffffffu, mbar_wait(&c.pfree[h], (t - 1) & 1u, ctl)) && okw;
+                    if (t > 0)
+                        okw = __all_sync(0xffffffffu, pfree_seen || mbar_wait(&c.pfree[h], (t - 1) & 1u, ctl)) && okw;
                     // O must hold every earlier unit of this range before it is rescaled.
                     if ((i > 0 || h > 0) && __any_sync(0xffffffffu, move)) {
                         const bool prev = h == 1 ? mbar_wait(&c.pfree[0], t & 1u, ctl)
