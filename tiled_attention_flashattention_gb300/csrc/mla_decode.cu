@@ -625,10 +625,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // Send buffer h was last read by the copy of unit (t - 1, h)
                     // (at most the other buffer's copy may still be pending) and
                     // by this CTA's softmax.
-                    bool got = true;
+                    // (both buffers' barriers tested together first: a wait costs
+                    // ~170 cycles even on a completed phase)
+                    bool got = true, xfree_seen = true;
                     if (leader && t > 0) {
+                        const bool own_seen = mbar_poll(smem_u32(&c.own_free[h]), (t - 1) & 1u);
+                        xfree_seen = mbar_poll(smem_u32(&c.xfree[h]), (t - 1) & 1u);
                         bulk_wait_read_allow1();
-                        got = mbar_wait(&c.own_free[h], (t - 1) & 1u, ctl);
+                        got = own_seen || mbar_wait(&c.own_free[h], (t - 1) & 1u, ctl);
                     }
                     if (leader) MLA_TRACE(kTrSendBuf0 + h, static_cast<int>(t));
                     if (!(ok = barrier_and(kBarX, 128, got))) break;
@@ -642,7 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     named_barrier(kBarX, 128);
                     if (leader) {
                         // The peer's receive buffer h is free once its softmax read unit (t - 1, h).
-                        if (t == 0 || mbar_wait(&c.xfree[h], (t - 1) & 1u, ctl)) {
+                        if (t == 0 || xfree_seen || mbar_wait(&c.xfree[h], (t - 1) & 1u, ctl)) {
                             mbar_arrive_expect_tx(&c.xfull[h], kXBytes);   // the peer's unit (t, h)
                             bulk_copy_to_peer(peer_recv[h], sSend + h * kXBytes, kXBytes, peer_xfull[h]);
                             bulk_commit_group();
