@@ -344,6 +344,38 @@ int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void
 #define GBATTN_MLA_TRACE_BYTES (8 * 2 * GBATTN_MLA_TRACE_EVENTS * GBATTN_MLA_TRACE_TILES)
 int gbattn_mla_trace(void *host, size_t bytes);
 
+/*
+ * gbattn_attn_trace -- latency trace of the prefill kernel's two-Q-tile form
+ * (observability; the pages have no counterpart).  Only the trace build
+ * (-DGBATTN_TRACE) records it; the default library returns
+ * GBATTN_ERR_UNSUPPORTED and writes nothing.
+ *
+ * In the trace build every launch of attn_fwd that takes the two-tile form
+ * (two 128-row query tiles per CTA, 128-key tiles) stamps, for four CTAs
+ * (blocks 0, 1, grid / 3 and 2 grid / 3) and the first GBATTN_ATTN_TRACE_TILES
+ * key blocks of each, the SM cycle counter at each step of a key block's chain.
+ * This call synchronises the device, copies the stamps of the launches since
+ * the last call to `host` and clears them.  Layout: int64
+ * [GBATTN_ATTN_TRACE_CTAS][GBATTN_ATTN_TRACE_EVENTS][GBATTN_ATTN_TRACE_TILES]
+ * (cycles; tile = key block - the CTA's first key block; 0 = not reached),
+ * followed by int64 [GBATTN_ATTN_TRACE_CTAS][4]: each CTA's cycle counter and
+ * global timer (ns) at its start, then at its end.  Events, in order (issuer:
+ * tile j's V awaited, V seen, P of Q tile 0 seen, P V of Q tile 0 issued, K of
+ * tile j + 1 seen, S of Q tile 0 for tile j + 1 issued, P of Q tile 1 seen, P V
+ * of Q tile 1 issued, S of Q tile 1 for tile j + 1 issued; then for each Q tile's
+ * softmax warpgroup: S seen, scores loaded, row maximum, exponentials and P
+ * stored, P-ready arrive).
+ *   host: caller-owned, at least GBATTN_ATTN_TRACE_BYTES bytes.
+ * Errors: GBATTN_ERR_UNSUPPORTED (default library), GBATTN_ERR_INVALID_ARG
+ * (host NULL or bytes too small), GBATTN_ERR_LAUNCH.
+ */
+#define GBATTN_ATTN_TRACE_CTAS 4
+#define GBATTN_ATTN_TRACE_EVENTS 19
+#define GBATTN_ATTN_TRACE_TILES 132
+#define GBATTN_ATTN_TRACE_BYTES \
+    (8 * GBATTN_ATTN_TRACE_CTAS * (GBATTN_ATTN_TRACE_EVENTS * GBATTN_ATTN_TRACE_TILES + 4))
+int gbattn_attn_trace(void *host, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -170,3 +170,5 @@ def test_default_library_has_no_latency_trace(lib):
     # library answers UNSUPPORTED without touching the device
     assert lib.gbattn_mla_trace(None, 0) == 2
     assert b"GBATTN_TRACE" in lib.gbattn_last_error()
+    assert lib.gbattn_attn_trace(None, 0) == 2
+    assert b"GBATTN_TRACE" in lib.gbattn_last_error()

@@ -1,6 +1,7 @@
-"""The MLA decode latency trace: the trace build (-DGBATTN_TRACE) computes
-bit-identical results to the default library and stamps every step of each
-traced tile's chain in the order the kernel's dependencies force."""
+"""The latency traces of the MLA decode kernel and of the prefill kernel's
+two-tile form: the trace build (-DGBATTN_TRACE) computes bit-identical results
+to the default library and stamps every step of each traced tile's chain in the
+order the kernel's dependencies force."""
 import os
 import subprocess
 import sys
@@ -78,3 +79,66 @@ def test_trace_build_matches_and_stamps_in_order(tmp_path):
             assert (s(f"softmax{h}_in") <= s(f"p{h}_ready")).all()
             assert (s(f"p{h}_ready") <= s(f"pv{h}_issue")).all()   # P V waits for P
         assert (np.diff(s("s_issue")) > 0).all()           # tiles in order
+
+
+# Prefill: causal, N = 4096, two heads -> the two-tile form (a 128-row query
+# tile visits 16.5 key tiles on average), grid 32, traced blocks 0, 1, 10, 21.
+PN, PH = 4096, 2
+CHILD_ATTN = f"""
+import sys, numpy as np, torch
+sys.path.insert(0, {ROOT!r})
+import tiled_attention_flashattention_gb300 as gb
+from tiled_attention_flashattention_gb300 import _build, workloads as wl
+_build.build(trace=True)
+gb.load_library(trace=True)
+Q, K, V = (t.cuda() for t in wl.random_prefill(1, {PH}, {PH}, {PN}, {PN}, 128, seed=12))
+gb.attn_fwd(Q, K, V, causal=True, scale=0.088); gb.check(); gb.attn_trace()
+O, L = gb.attn_fwd(Q, K, V, causal=True, scale=0.088); gb.check()
+tr, clock = gb.attn_trace()
+np.savez(sys.argv[1], O=O.view(torch.int16).cpu().numpy(), L=L.cpu().numpy(), tr=tr, clock=clock)
+"""
+
+
+def test_default_library_reports_unsupported_attn():
+    with pytest.raises(gb.GbattnError) as e:
+        gb.attn_trace()
+    assert e.value.code == 2
+
+
+def test_attn_trace_build_matches_and_stamps_in_order(tmp_path):
+    out = str(tmp_path / "trace_attn.npz")
+    r = subprocess.run([sys.executable, "-c", CHILD_ATTN, out], capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    d = np.load(out)
+    Q, K, V = (t.cuda() for t in wl.random_prefill(1, PH, PH, PN, PN, 128, seed=12))
+    O, L = gb.attn_fwd(Q, K, V, causal=True, scale=0.088)
+    gb.check()
+    assert np.array_equal(d["O"], O.view(torch.int16).cpu().numpy())
+    assert np.array_equal(d["L"], L.cpu().numpy())
+    tr, clock = d["tr"], d["clock"]
+    ev = {n: i for i, n in enumerate(gb.ATTN_TRACE_EVENTS)}
+    # blocks 0 / 1 / 10 / 21 take 256-row query blocks 15 / 15 / 10 / 5 (longest
+    # first over the two heads): 32 / 32 / 22 / 12 key tiles
+    for cta, ntile in enumerate((32, 32, 22, 12)):
+        x = tr[cta]
+        assert clock[cta, 2] > clock[cta, 0] and clock[cta, 3] > clock[cta, 1]
+        n = int(np.sum(x[ev["v_seen"]] > 0))
+        assert n == ntile, (cta, n)
+        s = lambda e, a=0, b=None: x[ev[e], a:(n if b is None else b)]
+        assert (np.diff(s("v_seen")) > 0).all()              # tiles in order
+        assert (s("wait_v") <= s("v_seen")).all()
+        assert (s("v_seen", 0, n - 1) <= s("p0_seen", 0, n - 1)).all()
+        for t in (0, 1):
+            # Q tile 0 of a causal two-tile block ends one key tile before Q tile 1
+            m = n - 1 if t == 0 else n
+            assert (s(f"s{t}_seen", 0, m) <= s(f"s{t}_loaded", 0, m)).all()
+            assert (s(f"s{t}_loaded", 0, m) <= s(f"max{t}", 0, m)).all()
+            assert (s(f"max{t}", 0, m) <= s(f"exp{t}", 0, m)).all()
+            assert (s(f"exp{t}", 0, m) <= s(f"p{t}_arrive", 0, m)).all()
+            # the issuer sees P only after the softmax's arrive, then issues P V
+            assert (s(f"p{t}_arrive", 0, m) <= s(f"p{t}_seen", 0, m)).all()
+            assert (s(f"p{t}_seen", 0, m) <= s(f"pv{t}_issued", 0, m)).all()
+            # the softmax sees the next tile's S only after the issuer issued it
+            nxt = "s0_next_issued" if t == 0 else "s1_next_issued"
+            assert (s(nxt, 0, m - 1) <= s(f"s{t}_seen", 1, m)).all()
+

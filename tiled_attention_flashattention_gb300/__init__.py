@@ -19,7 +19,7 @@ import torch
 __all__ = ["attn_fwd", "attn_fwd_sparse", "mla_decode", "mla_decode_workspace_bytes", "mla_decode_paged",
            "mla_decode_paged_workspace_bytes", "mla_decode_noalloc", "ssd_scan", "attn_fwd_host",
            "attn_fwd_host_device_bytes", "mla_decode_host", "mla_decode_host_device_bytes",
-           "check", "selftest_umma", "mla_trace", "MLA_TRACE_EVENTS",
+           "check", "selftest_umma", "mla_trace", "MLA_TRACE_EVENTS", "attn_trace", "ATTN_TRACE_EVENTS",
            "set_wait_timeout_ns", "set_fault_injection", "GbattnError", "library_path", "load_library"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -97,6 +97,8 @@ def load_library(trace: bool = False):
         lib.gbattn_selftest_umma.restype = I
         lib.gbattn_mla_trace.argtypes = [P, SZ]
         lib.gbattn_mla_trace.restype = I
+        lib.gbattn_attn_trace.argtypes = [P, SZ]
+        lib.gbattn_attn_trace.restype = I
         _lib = lib
         _lib_trace = trace
         return lib
@@ -465,3 +467,26 @@ def mla_trace():
     buf = np.zeros((2, len(MLA_TRACE_EVENTS), _MLA_TRACE_TILES), dtype=np.uint64)
     _raise_if(load_library().gbattn_mla_trace(ctypes.c_void_p(buf.ctypes.data), buf.nbytes))
     return buf
+
+
+# Layout of gbattn_attn_trace (include/gbattn.h): int64 [4 CTAs][events][132
+# tiles] of SM cycles (0 = not reached), then int64 [4 CTAs][4]: cycles and ns at
+# each traced CTA's start and end.  Tile j's "k_next_seen", "s0_next_issued" and
+# "s1_next_issued" refer to key tile j + 1.
+ATTN_TRACE_EVENTS = ("wait_v", "v_seen", "p0_seen", "pv0_issued", "k_next_seen", "s0_next_issued", "p1_seen",
+                     "pv1_issued", "s1_next_issued", "s0_seen", "s0_loaded", "max0", "exp0", "p0_arrive", "s1_seen",
+                     "s1_loaded", "max1", "exp1", "p1_arrive")
+_ATTN_TRACE_CTAS = 4
+_ATTN_TRACE_TILES = 132
+
+
+def attn_trace():
+    """Stamps of the two-tile prefill launches since the last call (trace build
+    only: ``load_library(trace=True)``): (cycles int64 [4, 19, 132], clock int64
+    [4, 4]); clears them."""
+    import numpy as np
+    n0 = _ATTN_TRACE_CTAS * len(ATTN_TRACE_EVENTS) * _ATTN_TRACE_TILES
+    buf = np.zeros(n0 + _ATTN_TRACE_CTAS * 4, dtype=np.int64)
+    _raise_if(load_library().gbattn_attn_trace(ctypes.c_void_p(buf.ctypes.data), buf.nbytes))
+    return (buf[:n0].reshape(_ATTN_TRACE_CTAS, len(ATTN_TRACE_EVENTS), _ATTN_TRACE_TILES),
+            buf[n0:].reshape(_ATTN_TRACE_CTAS, 4))

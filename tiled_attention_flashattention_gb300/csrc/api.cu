@@ -795,6 +795,14 @@ extern "C" int gbattn_mla_trace(void *host, size_t bytes)
     return GBATTN_OK;
 }
 
+extern "C" int gbattn_attn_trace(void *host, size_t bytes)
+{
+    std::string err;
+    const int rc = attn_trace_fetch(host, bytes, err);
+    if (rc != GBATTN_OK) return fail(rc, err);
+    return GBATTN_OK;
+}
+
 extern "C" int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void *V, float *S,
                                     float *O, void *stream)
 {

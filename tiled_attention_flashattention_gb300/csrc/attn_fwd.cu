@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "gbattn.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -136,6 +137,55 @@ struct Range {
     int lo, hi;         // KV tiles [lo, hi); empty when lo >= hi
 };
 
+// Event stamps for latency studies of the two-tile form, compiled in only with
+// -DGBATTN_TRACE (the library's trace build): for four CTAs of a launch (blocks
+// 0, 1, grid / 3 and 2 grid / 3) the SM cycle counter at each step of every key
+// tile's chain, [CTA][event][tile], tile = key block - the CTA's first block,
+// 0 = not reached; plus each CTA's cycle counter and global timer (ns) at its
+// start and end, which convert cycles to time.  The events are listed with
+// gbattn_attn_trace in the public header.
+enum AttnTraceEvent : int {
+    kAtWaitV = 0, kAtVSeen, kAtP0Seen, kAtPV0Issued, kAtKNextSeen, kAtS0NextIssued, kAtP1Seen, kAtPV1Issued,
+    kAtS1NextIssued, kAtS0Seen, kAtS0Loaded, kAtMax0, kAtExp0, kAtP0Arrive, kAtS1Seen, kAtS1Loaded, kAtMax1,
+    kAtExp1, kAtP1Arrive, kAtEvents
+};
+constexpr int kAtCtas = 4;
+constexpr int kAtTiles = 132;
+#ifdef GBATTN_TRACE
+__device__ long long g_attn_trace[kAtCtas][kAtEvents][kAtTiles];
+__device__ long long g_attn_trace_clock[kAtCtas][4];   // cycles, ns at the CTA's start; cycles, ns at its end
+__device__ __forceinline__ int attn_trace_slot()
+{
+    const unsigned g = gridDim.x, bx = blockIdx.x;
+    return bx == 0 ? 0 : bx == 1 ? 1 : bx == g / 3 ? 2 : bx == 2 * g / 3 ? 3 : -1;
+}
+#define ATTN_TRACE(e, i)                                                                 \
+    do {                                                                                 \
+        if constexpr (kT == 2 && !kSparse) {                                             \
+            const int s_ = attn_trace_slot();                                            \
+            if (s_ >= 0 && static_cast<unsigned>(i) < static_cast<unsigned>(kAtTiles))   \
+                g_attn_trace[s_][e][i] = clock64();                                      \
+        }                                                                                \
+    } while (0)
+#define ATTN_TRACE_CLOCK(k)                                                              \
+    do {                                                                                 \
+        if constexpr (kT == 2 && !kSparse) {                                             \
+            const int s_ = attn_trace_slot();                                            \
+            if (s_ >= 0) {                                                               \
+                g_attn_trace_clock[s_][2 * (k)] = clock64();                             \
+                g_attn_trace_clock[s_][2 * (k) + 1] = static_cast<long long>(global_timer_ns()); \
+            }                                                                            \
+        }                                                                                \
+    } while (0)
+#else
+#define ATTN_TRACE(e, i) \
+    do {                 \
+    } while (0)
+#define ATTN_TRACE_CLOCK(k) \
+    do {                    \
+    } while (0)
+#endif
+
 // BN-key tiles touched by query rows [r0, r1) (r1 > r0).
 template <int BN>
 __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
@@ -172,6 +222,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) ATTN_TRACE_CLOCK(0);
 
     // ---- work item: (batch, head, 128 kT-row query block), longest first
     const int nbh = p.B * p.H;
@@ -448,16 +499,20 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             };
             for (int j = first; j < hi && ok && !kPipe;) {
                 const int slotV = it % C::kSlots;
+                ATTN_TRACE(kAtWaitV, j - first);
                 if (!v_seen && !(ok = mbar_wait(&c.full[slotV], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                     break;
                 ++it;
+                ATTN_TRACE(kAtVSeen, j - first);
                 // (item `it` is the next block's K when there is one; otherwise the
                 // test's result is not used)
                 const bool k_seen = !kSparse && ring_poll(it);
                 if (act(0, j)) {
                     if (!(ok = mbar_wait(&c.p_full[0], pcount[0]++ & 1u, ctl))) break;
+                    ATTN_TRACE(kAtP0Seen, j - first);
                     tc_fence_after_sync();
                     issue_PV(0, 0, slotV);
+                    ATTN_TRACE(kAtPV0Issued, j - first);
                 }
                 const int jn = next_any(j);
                 int slotK = -1;
@@ -467,22 +522,27 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     if (!k_seen && !(ok = mbar_wait(&c.full[slotK], static_cast<uint32_t>(it / C::kSlots) & 1u, ctl)))
                         break;
                     ++it;
+                    ATTN_TRACE(kAtKNextSeen, j - first);
                     v_seen = !kSparse && ring_poll(it);
                     if (act(0, jn)) {
                         issue_S(0, 0, slotK);
                         umma_commit(&c.s_full[0]);
+                        ATTN_TRACE(kAtS0NextIssued, j - first);
                     }
                 }
                 if (act(1, j)) {
                     if (!(ok = mbar_wait(&c.p_full[1], pcount[1]++ & 1u, ctl))) break;
+                    ATTN_TRACE(kAtP1Seen, j - first);
                     tc_fence_after_sync();
                     issue_PV(1, 1, slotV);
+                    ATTN_TRACE(kAtPV1Issued, j - first);
                 }
                 umma_commit(&c.empty[slotV]);
                 if (slotK >= 0) {
                     if (act(1, jn)) {
                         issue_S(1, 1, slotK);
                         umma_commit(&c.s_full[1]);
+                        ATTN_TRACE(kAtS1NextIssued, j - first);
                     }
                     umma_commit(&c.empty[slotK]);
                 }
@@ -532,6 +592,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             // tcgen05.ld/st below are warp-collective: keep the outcome warp-uniform.
             ok = __all_sync(0xffffffffu, mbar_wait(&c.s_full[sb], sphase, ctl));
             if (!ok) break;
+            if (quad == 0 && lane == 0) ATTN_TRACE(kAtS0Seen + 5 * t, j - first);
             tc_fence_after_sync();
             float s[BN];
             {
@@ -543,6 +604,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
 #pragma unroll
                 for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
             }
+            if (quad == 0 && lane == 0) ATTN_TRACE(kAtS0Loaded + 5 * t, j - first);
 
             const int k0 = j * BN;
             const bool need_mask = (k0 + BN > p.N_kv) || (k0 + BN - 1 > r0[t] + off + p.hi_pad) ||
@@ -579,6 +641,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                 if (i < BN) m4[q] = fmaxf(m4[q], s[i]);
             }
             const float mx = max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+            if (quad == 0 && lane == 0) ATTN_TRACE(kAtMax0 + 5 * t, j - first);
 
             const bool move = mx > m_ref + thr;
             const float new_ref = move ? mx : m_ref;
@@ -604,6 +667,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                 }
                 tmem_st_x16(tS + q * 16, pk);
             }
+            if (quad == 0 && lane == 0) ATTN_TRACE(kAtExp0 + 5 * t, j - first);
             {
                 float a0, a1;
                 f2_unpack(add_f2(sum2[0], sum2[1]), a0, a1);
@@ -631,6 +695,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             }
             tmem_st_wait();
             tc_fence_before_sync();
+            if (quad == 0 && lane == 0) ATTN_TRACE(kAtP0Arrive + 5 * t, j - first);
             mbar_arrive(&c.p_full[sb]);
         }
 
@@ -689,6 +754,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
         tc_fence_after_sync();
         tmem_dealloc(tbase, C::kTmemCols);
     }
+    if (threadIdx.x == 0) ATTN_TRACE_CLOCK(1);
 }
 
 template <int D, bool kSparse, int kT, int BN = kBN>
@@ -813,6 +879,40 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
                         : launch<64, false, 1, 64>(tq, tk, tv, to, p, g, env, err);
     return d == 128 ? launch<128, false, 2>(tq, tk, tv, to, p, g, env, err)
                     : launch<64, false, 2>(tq, tk, tv, to, p, g, env, err);
+}
+
+int attn_trace_fetch(void *host, size_t bytes, std::string &err)
+{
+#ifdef GBATTN_TRACE
+    static_assert(kAtEvents == GBATTN_ATTN_TRACE_EVENTS && kAtTiles == GBATTN_ATTN_TRACE_TILES &&
+                      kAtCtas == GBATTN_ATTN_TRACE_CTAS,
+                  "trace layout of the public header");
+    constexpr size_t n0 = sizeof(g_attn_trace), n1 = sizeof(g_attn_trace_clock);
+    static_assert(n0 + n1 == GBATTN_ATTN_TRACE_BYTES, "trace size of the public header");
+    if (host == nullptr || bytes < n0 + n1) {
+        err = "gbattn_attn_trace: host buffer missing or smaller than GBATTN_ATTN_TRACE_BYTES";
+        return GBATTN_ERR_INVALID_ARG;
+    }
+    void *d0 = nullptr, *d1 = nullptr;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(host, g_attn_trace, n0);
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(static_cast<char *>(host) + n0, g_attn_trace_clock, n1);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&d0, g_attn_trace);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&d1, g_attn_trace_clock);
+    if (e == cudaSuccess) e = cudaMemset(d0, 0, n0);
+    if (e == cudaSuccess) e = cudaMemset(d1, 0, n1);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        err = std::string("gbattn_attn_trace: ") + cudaGetErrorString(e);
+        return GBATTN_ERR_LAUNCH;
+    }
+    return GBATTN_OK;
+#else
+    (void)host;
+    (void)bytes;
+    err = "gbattn_attn_trace: this library was built without GBATTN_TRACE";
+    return GBATTN_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // namespace gbattn

@@ -73,6 +73,11 @@ int launch_mla_decode_noalloc(const void *Q_nope, const void *Q_pe, const void *
 // the trace build; returns a gbattn_status value (UNSUPPORTED otherwise).
 int mla_trace_fetch(void *host, size_t bytes, std::string &err);
 
+// Prefill latency trace (gbattn_attn_trace): copies and clears the two-tile
+// form's stamps of the trace build; returns a gbattn_status value
+// (UNSUPPORTED otherwise).
+int attn_trace_fetch(void *host, size_t bytes, std::string &err);
+
 // Mamba-2 SSD scan (ssd_scan).
 int launch_ssd_scan(const void *x, const float *dt, const float *A, const void *Bm, const void *Cm, const float *D,
                     float *y, float *S_final, int Bsz, int L, int H, int P, int G, int N, const LaunchEnv &env,
