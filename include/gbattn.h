@@ -345,13 +345,14 @@ int gbattn_selftest_umma(const void *A, const void *B, const void *P, const void
 int gbattn_mla_trace(void *host, size_t bytes);
 
 /*
- * gbattn_attn_trace -- latency trace of the prefill kernel's two-Q-tile form
+ * gbattn_attn_trace -- latency trace of the prefill kernel's dense forms
  * (observability; the pages have no counterpart).  Only the trace build
  * (-DGBATTN_TRACE) records it; the default library returns
  * GBATTN_ERR_UNSUPPORTED and writes nothing.
  *
- * In the trace build every launch of attn_fwd that takes the two-tile form
- * (two 128-row query tiles per CTA, 128-key tiles) stamps, for four CTAs
+ * In the trace build every launch of attn_fwd (the two-tile form: two 128-row
+ * query tiles per CTA, 128-key tiles; or the pipelined one-tile form: one
+ * query tile, 64-key tiles, which stamps the Q tile 0 events only) stamps, for four CTAs
  * (blocks 0, 1, grid / 3 and 2 grid / 3) and the first GBATTN_ATTN_TRACE_TILES
  * key blocks of each, the SM cycle counter at each step of a key block's chain.
  * This call synchronises the device, copies the stamps of the launches since

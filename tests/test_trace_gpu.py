@@ -142,3 +142,44 @@ def test_attn_trace_build_matches_and_stamps_in_order(tmp_path):
             nxt = "s0_next_issued" if t == 0 else "s1_next_issued"
             assert (s(nxt, 0, m - 1) <= s(f"s{t}_seen", 1, m)).all()
 
+
+# Prefill, pipelined one-tile form: causal N = 1024, two heads (a query tile
+# visits 4.5 key tiles of 128 on average), grid 16, traced blocks 0, 1, 5, 10.
+def test_attn_trace_pipelined_form_stamps_in_order(tmp_path):
+    out = str(tmp_path / "trace_pipe.npz")
+    child = CHILD_ATTN.replace(f"{PN}, {PN}, 128, seed=12", "1024, 1024, 128, seed=13")
+    assert child != CHILD_ATTN
+    r = subprocess.run([sys.executable, "-c", child, out], capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    d = np.load(out)
+    Q, K, V = (t.cuda() for t in wl.random_prefill(1, PH, PH, 1024, 1024, 128, seed=13))
+    O, L = gb.attn_fwd(Q, K, V, causal=True, scale=0.088)
+    gb.check()
+    assert np.array_equal(d["O"], O.view(torch.int16).cpu().numpy())
+    assert np.array_equal(d["L"], L.cpu().numpy())
+    tr = d["tr"]
+    ev = {n: i for i, n in enumerate(gb.ATTN_TRACE_EVENTS)}
+    # blocks 0 / 1 / 5 / 10 take 128-row query blocks 7 / 7 / 5 / 2: 16 / 16 / 12 / 6
+    # key tiles of 64; one Q tile, so no Q tile 1 events
+    for cta, ntile in enumerate((16, 16, 12, 6)):
+        x = tr[cta]
+        n = int(np.sum(x[ev["v_seen"]] > 0))
+        assert n == ntile, (cta, n)
+        for e in ("p1_seen", "pv1_issued", "s1_next_issued", "s1_seen", "p1_arrive"):
+            assert not (x[ev[e]] > 0).any()
+        s = lambda e, a=0, b=None: x[ev[e], a:(n if b is None else b)]
+        assert (np.diff(s("v_seen")) > 0).all()
+        assert (s("wait_v") <= s("v_seen")).all()
+        assert (s("s0_seen") <= s("s0_loaded")).all()
+        assert (s("s0_loaded") <= s("max0")).all()
+        assert (s("max0") <= s("exp0")).all()
+        assert (s("exp0") <= s("p0_arrive")).all()
+        assert (s("p0_arrive") <= s("p0_seen")).all()
+        assert (s("p0_seen") <= s("pv0_issued")).all()
+        # S of tile n + 1 is issued once its K landed and then seen by the softmax
+        # (before or after P V of tile n, whichever had its inputs first)
+        assert (s("k_next_seen", 0, n - 1) <= s("s0_next_issued", 0, n - 1)).all()
+        assert (s("s0_next_issued", 0, n - 1) <= s("s0_seen", 1, n)).all()
+        # and not before P V of tile n - 1 (it overwrites that P's buffer)
+        assert (s("pv0_issued", 0, n - 2) <= s("s0_next_issued", 1, n - 1)).all()
+

@@ -481,7 +481,7 @@ _ATTN_TRACE_TILES = 132
 
 
 def attn_trace():
-    """Stamps of the two-tile prefill launches since the last call (trace build
+    """Stamps of the dense prefill launches since the last call (trace build
     only: ``load_library(trace=True)``): (cycles int64 [4, 19, 132], clock int64
     [4, 4]); clears them."""
     import numpy as np

@@ -137,13 +137,14 @@ struct Range {
     int lo, hi;         // KV tiles [lo, hi); empty when lo >= hi
 };
 
-// Event stamps for latency studies of the two-tile form, compiled in only with
-// -DGBATTN_TRACE (the library's trace build): for four CTAs of a launch (blocks
-// 0, 1, grid / 3 and 2 grid / 3) the SM cycle counter at each step of every key
-// tile's chain, [CTA][event][tile], tile = key block - the CTA's first block,
-// 0 = not reached; plus each CTA's cycle counter and global timer (ns) at its
-// start and end, which convert cycles to time.  The events are listed with
-// gbattn_attn_trace in the public header.
+// Event stamps for latency studies of the dense forms (two-tile and pipelined
+// one-tile), compiled in only with -DGBATTN_TRACE (the library's trace build):
+// for four CTAs of a launch (blocks 0, 1, grid / 3 and 2 grid / 3) the SM cycle
+// counter at each step of every key tile's chain, [CTA][event][tile], tile =
+// key block - the CTA's first block, 0 = not reached; plus each CTA's cycle
+// counter and global timer (ns) at its start and end, which convert cycles to
+// time.  The events are listed with gbattn_attn_trace in the public header (the
+// pipelined form has one Q tile: it stamps the tile-0 events only).
 enum AttnTraceEvent : int {
     kAtWaitV = 0, kAtVSeen, kAtP0Seen, kAtPV0Issued, kAtKNextSeen, kAtS0NextIssued, kAtP1Seen, kAtPV1Issued,
     kAtS1NextIssued, kAtS0Seen, kAtS0Loaded, kAtMax0, kAtExp0, kAtP0Arrive, kAtS1Seen, kAtS1Loaded, kAtMax1,
@@ -161,7 +162,7 @@ __device__ __forceinline__ int attn_trace_slot()
 }
 #define ATTN_TRACE(e, i)                                                                 \
     do {                                                                                 \
-        if constexpr (kT == 2 && !kSparse) {                                             \
+        if constexpr (!kSparse) {                                                        \
             const int s_ = attn_trace_slot();                                            \
             if (s_ >= 0 && static_cast<unsigned>(i) < static_cast<unsigned>(kAtTiles))   \
                 g_attn_trace[s_][e][i] = clock64();                                      \
@@ -169,7 +170,7 @@ __device__ __forceinline__ int attn_trace_slot()
     } while (0)
 #define ATTN_TRACE_CLOCK(k)                                                              \
     do {                                                                                 \
-        if constexpr (kT == 2 && !kSparse) {                                             \
+        if constexpr (!kSparse) {                                                        \
             const int s_ = attn_trace_slot();                                            \
             if (s_ >= 0) {                                                               \
                 g_attn_trace_clock[s_][2 * (k)] = clock64();                             \
@@ -454,18 +455,24 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     if (n + 1 < ntile) {
                         const int ik = it++;
                         if (!(ok = mbar_wait(&c.full[islot(ik)], iphase(ik), ctl))) break;
+                        ATTN_TRACE(kAtKNextSeen, n);
                         tc_fence_after_sync();
                         issue_S(0, (n + 1) & 1, islot(ik));
                         umma_commit(&c.s_full[(n + 1) & 1]);
                         umma_commit(&c.empty[islot(ik)]);
+                        ATTN_TRACE(kAtS0NextIssued, n);
                     }
                     const int iv = it++;
+                    ATTN_TRACE(kAtWaitV, n);
                     if (!(ok = mbar_wait(&c.full[islot(iv)], iphase(iv), ctl))) break;
+                    ATTN_TRACE(kAtVSeen, n);
                     // P of tile n: one barrier per S buffer (the softmax may already have
                     // finished tile n + 1, whose S was issued above)
                     if (!(ok = mbar_wait(&c.p_full[n & 1], static_cast<uint32_t>(n >> 1) & 1u, ctl))) break;
+                    ATTN_TRACE(kAtP0Seen, n);
                     tc_fence_after_sync();
                     issue_PV(0, n & 1, islot(iv));
+                    ATTN_TRACE(kAtPV0Issued, n);
                     umma_commit(&c.empty[islot(iv)]);
                     umma_commit(&c.pv_done);
                 }

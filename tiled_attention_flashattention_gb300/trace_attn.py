@@ -1,4 +1,4 @@
-"""Latency trace of the prefill kernel's two-tile form on the GPU (observability tool).
+"""Latency trace of the prefill kernel's dense forms on the GPU (observability tool).
 
     python -m tiled_attention_flashattention_gb300.trace_attn [--workload NAME] [--table]
 
@@ -14,11 +14,13 @@ the delay from S issued to S seen, the score load, the row maximum, the
 exponentials with the P stores, the wait for the stores and the arrive, and
 the delays from the arrive to the issuer seeing P and to the next S being
 seen.  Cycles are converted to time with each CTA's own cycle / global-timer
-ratio.  ``--table`` also prints every tile's stamps.
+ratio.  ``--table`` also prints every tile's stamps.  Launches that take the
+two-tile form (long rows) and the pipelined one-tile form (short rows: one Q
+tile, 64-key tiles, S of tile n + 1 issued before P V of tile n) are traced;
+block-sparse launches are not.
 
 Runs in a process of its own: the trace build and the default library export
-the same symbols and are not loaded together.  Only launches that take the
-two-tile form record stamps (the launcher's choice for long rows).
+the same symbols and are not loaded together.
 """
 from __future__ import annotations
 
@@ -34,11 +36,13 @@ from . import workloads as wl
 
 def steady_state_summary(tr: np.ndarray, clock: np.ndarray, cta: int) -> dict:
     """Medians (cycles) of a traced CTA's per-tile steps over its reached tiles,
-    less the first and last quarter, plus the CTA's clock (GHz)."""
+    less the first and last quarter, plus the CTA's clock (GHz) and its form
+    ("two-tile" or "pipelined", from which events it stamped)."""
     ev = {n: i for i, n in enumerate(ATTN_TRACE_EVENTS)}
     x = tr[cta].astype(np.float64)
     n = int(np.sum(x[ev["v_seen"]] > 0))
-    out = {"tiles": n}
+    pipelined = not (x[ev["s1_seen"]] > 0).any()
+    out = {"tiles": n, "form": "pipelined" if pipelined else "two-tile"}
     c0, t0, c1, t1 = (float(v) for v in clock[cta])
     out["ghz"] = (c1 - c0) / (t1 - t0) if t1 > t0 else float("nan")
     lo, hi = n // 4, n - n // 4
@@ -52,6 +56,25 @@ def steady_state_summary(tr: np.ndarray, clock: np.ndarray, cta: int) -> dict:
     def med(v):
         return float(np.median(v))
 
+    if pipelined:
+        # issuer per tile n: K(n + 1) seen, S(n + 1) issued, V(n) seen, P(n) seen, P V(n) issued
+        out.update({
+            "period": med(np.diff(g("v_seen", slice(lo, hi + 1)))),
+            "issuer: wait next K": med(g("k_next_seen", r1) - g("pv0_issued")),
+            "issuer: issue next S": med(g("s0_next_issued") - g("k_next_seen")),
+            "issuer: wait V": med(g("v_seen") - g("wait_v")),
+            "issuer: wait P": med(g("p0_seen") - g("v_seen")),
+            "issuer: issue P V": med(g("pv0_issued") - g("p0_seen")),
+            "softmax: S issued -> seen": med(g("s0_seen", r1) - g("s0_next_issued")),
+            "softmax: load scores": med(g("s0_loaded") - g("s0_seen")),
+            "softmax: row max": med(g("max0") - g("s0_loaded")),
+            "softmax: exp2, P stores": med(g("exp0") - g("max0")),
+            "softmax: wait stores, arrive": med(g("p0_arrive") - g("exp0")),
+            "softmax: arrive -> issuer sees P": med(g("p0_seen") - g("p0_arrive")),
+            "softmax: arrive -> next S seen": med(g("s0_seen", r1) - g("p0_arrive")),
+            "V seen - P arrive": med(g("v_seen") - g("p0_arrive")),
+        })
+        return out
     out.update({
         "period": med(np.diff(g("v_seen", slice(lo, hi + 1)))),
         "issuer: wait V": med(g("v_seen") - g("wait_v")),
@@ -97,14 +120,14 @@ def main(argv=None):
     attn_fwd(Q, K, V, causal=c.causal, window=c.window, scale=c.softmax_scale())
     check()
     tr, clock = attn_trace()
-    print(f"{c.name}: two-tile trace of 4 CTAs")
+    print(f"{c.name}: trace of 4 CTAs")
     for cta in range(tr.shape[0]):
         sm = steady_state_summary(tr, clock, cta)
         if sm["tiles"] == 0:
-            print(f"  CTA slot {cta}: not traced (the launch did not take the two-tile form)")
+            print(f"  CTA slot {cta}: not traced")
             continue
         ghz = sm.pop("ghz")
-        print(f"  CTA slot {cta}: {sm.pop('tiles')} key tiles, SM clock {ghz:.2f} GHz")
+        print(f"  CTA slot {cta}: {sm.pop('form')} form, {sm.pop('tiles')} key tiles, SM clock {ghz:.2f} GHz")
         for k, v in sm.items():
             print(f"    {k:40s} {v:7.0f} cycles {v / ghz / 1000:6.3f} us")
         if args.table:
