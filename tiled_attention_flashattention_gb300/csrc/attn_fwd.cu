@@ -68,8 +68,9 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (producer, MMA issuer, idle warps) gives registers to the softmax
 // warpgroups, which hold a 128-float score row per thread.  kT = 2:
 // 128 * 104 + 256 * 200 = 64,512 = 384 * 168; kT = 1: 128 * 64 + 128 * 192
-// (or 56 + 200 where that avoids spills) = 32,768 = 256 * 128, the registers
-// each block is launched with.
+// (or 56 + 200 where that avoids spills; the pipelined forms, whose row is 64
+// floats, 88 + 168) = 32,768 = 256 * 128, the registers each block is launched
+// with.
 // BN keys per K/V tile: 128, or 64 for the pipelined one-tile form (kT = 1,
 // kPipe): its two 64-column S buffers let the score MMA of key tile j + 1 run
 // while the softmax works on tile j, inside one CTA, and two such CTAs still
@@ -206,12 +207,11 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
 {
     using C = Cfg<D, kT, BN>;
     constexpr bool kPipe = C::kPipe;
-    static_assert(!kSparse || BN == kBN, "the block mask is in 128-key blocks");
     static_assert(kT == 1 || BN == kBN, "the two-tile form uses 128-key tiles");
-    constexpr bool kWideSoftmax = kT == 2 || (kSparse && D == 128);
+    constexpr bool kWideSoftmax = kT == 2 || (kSparse && D == 128 && !kPipe);
     // (the pipelined form's softmax holds a 64-float row: more go to the issuer)
-    constexpr uint32_t kRegsLow = kT == 2 ? 104 : (kWideSoftmax ? 56 : (C::kPipe ? 80 : 64));
-    constexpr uint32_t kRegsHigh = kWideSoftmax ? 200 : (C::kPipe ? 176 : 192);
+    constexpr uint32_t kRegsLow = kT == 2 ? 104 : (kWideSoftmax ? 56 : (C::kPipe ? 88 : 64));
+    constexpr uint32_t kRegsHigh = kWideSoftmax ? 200 : (C::kPipe ? 168 : 192);
     static_assert(kT == 2 ? 128 * kRegsLow + 256 * kRegsHigh <= 384 * 168
                           : 128 * kRegsLow + 128 * kRegsHigh == 256 * 128, "register split");
     extern __shared__ uint8_t smem_raw[];
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
     // does Q tile t compute key block j?
     auto act = [&](int t, int j) -> bool {
         if constexpr (kSparse)
-            return in_rng(t, j) && __ldg(mrow[t] + j) != 0;
+            return in_rng(t, j) && __ldg(mrow[t] + j * BN / kBN) != 0;   // mask blocks are 128 keys
         else
             return in_rng(t, j);
     };
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             for (int t = 0; t < 2; ++t) {
                 int f = 0x7fffffff, l = -1;
                 for (int j = rng[t].lo + lane; j < rng[t].hi; j += 32)
-                    if (__ldg(mrow[t] + j)) {
+                    if (__ldg(mrow[t] + j * BN / kBN)) {
                         f = min(f, j);
                         l = max(l, j);
                     }
@@ -348,21 +348,15 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             bool ok = true;
             int it = 0;
             if constexpr (kPipe) {
-                // The issuer's order: K of tile 0, then for each tile n the K of
-                // tile n + 1 (its S runs first) and the V of tile n; the last
-                // tile has no next K.
-                const int ntile = hi - first;
-                for (int q = 0; q < 2 * ntile && ok; ++q) {
-                    int kv, n;
-                    if (q == 0) {
-                        kv = 0, n = 0;
-                    } else if (q == 2 * ntile - 1) {
-                        kv = 1, n = ntile - 1;
-                    } else if (q & 1) {
-                        kv = 0, n = (q + 1) / 2;
-                    } else {
-                        kv = 1, n = q / 2 - 1;
-                    }
+                // The issuer's order over the key tiles the CTA computes (all of
+                // [first, hi), or the active ones of a block mask): K of the
+                // first, then for each tile the K of the next one (its S runs
+                // first) and the V of this one; the last tile has no next K.
+                int jk = first, jv = first;      // tiles of the next K and the next V to load
+                bool k_turn = true;
+                while (jv < hi && ok) {
+                    const bool kv = !(k_turn && jk < hi);
+                    const int tile = kv ? jv : jk;
                     const int slot = it % C::kSlots;
                     const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
                     if (round > 0 && !(ok = mbar_wait(&c.empty[slot], (round & 1u) ^ 1u, ctl))) break;
@@ -370,8 +364,15 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     const CUtensorMap *m = kv ? &tmV : &tmK;
                     for (int ch = 0; ch < C::kChunks; ++ch)
                         tma_load_3d(ring + slot * C::kKvTileBytes + ch * C::kKvChunkBytes, m, &c.full[slot],
-                                    ch * 64, (first + n) * BN, kvh);
+                                    ch * 64, tile * BN, kvh);
                     ++it;
+                    if (kv) {
+                        jv = next_any(jv);
+                    } else {
+                        jk = next_any(jk);
+                    }
+                    // K(first) alone, then K(next), V(this) pairs
+                    k_turn = it == 1 ? true : !k_turn;
                 }
             } else {
                 for (int j = first; j < hi && ok; j = next_any(j)) {
@@ -440,19 +441,21 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                 // the other S buffer before P V of tile n, so it runs while the
                 // softmax works on tile n; that buffer's previous P was read by P V
                 // of tile n - 1, issued before it.
-                const int ntile = hi - first;
                 auto islot = [&](int i) { return i % C::kSlots; };
                 auto iphase = [&](int i) { return static_cast<uint32_t>(i / C::kSlots) & 1u; };
                 // ring items in the producer's order: K(0), then K(n + 1), V(n) per tile n
-                if (ok && ntile > 0 && (ok = mbar_wait(&c.full[islot(0)], iphase(0), ctl))) {
+                // (tiles n = the key tiles the CTA computes, in order)
+                int jcur = first;
+                if (ok && jcur < hi && (ok = mbar_wait(&c.full[islot(0)], iphase(0), ctl))) {
                     tc_fence_after_sync();
                     issue_S(0, 0, islot(0));
                     umma_commit(&c.s_full[0]);
                     umma_commit(&c.empty[islot(0)]);
                 }
                 it = 1;
-                for (int n = 0; n < ntile && ok; ++n) {
-                    if (n + 1 < ntile) {
+                for (int n = 0; jcur < hi && ok; ++n) {
+                    const int jn = next_any(jcur);
+                    if (jn < hi) {
                         const int ik = it++;
                         if (!(ok = mbar_wait(&c.full[islot(ik)], iphase(ik), ctl))) break;
                         ATTN_TRACE(kAtKNextSeen, n);
@@ -475,6 +478,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     ATTN_TRACE(kAtPV0Issued, n);
                     umma_commit(&c.empty[islot(iv)]);
                     umma_commit(&c.pv_done);
+                    jcur = jn;
                 }
             } else if (ok && first < hi) {
                 const int slotK = 0;
@@ -878,7 +882,10 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         return 2;
     }
     const int g = static_cast<int>(grid);
-    if (block_mask)   // always the one-tile form
+    // Block-sparse launches keep the one-tile form on 128-key tiles: the
+    // pipelined 64-key form (which also walks a block mask) measured 11 % slower
+    // at 25 % density, its scattered tiles paying the N = 64 score MMAs.
+    if (block_mask)
         return d == 128 ? launch<128, true, 1>(tq, tk, tv, to, p, g, env, err)
                         : launch<64, true, 1>(tq, tk, tv, to, p, g, env, err);
     if (kt == 1)
