@@ -151,9 +151,9 @@ enum AttnTraceEvent : int {
     kAtS1NextIssued, kAtS0Seen, kAtS0Loaded, kAtMax0, kAtExp0, kAtP0Arrive, kAtS1Seen, kAtS1Loaded, kAtMax1,
     kAtExp1, kAtP1Arrive, kAtEvents
 };
+#ifdef GBATTN_TRACE
 constexpr int kAtCtas = 4;
 constexpr int kAtTiles = 132;
-#ifdef GBATTN_TRACE
 __device__ long long g_attn_trace[kAtCtas][kAtEvents][kAtTiles];
 __device__ long long g_attn_trace_clock[kAtCtas][4];   // cycles, ns at the CTA's start; cycles, ns at its end
 __device__ __forceinline__ int attn_trace_slot()
