@@ -444,16 +444,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint64_t t_last = global_timer_ns();
             for (uint32_t spin = 1; gu < 2 * total; ++spin) {
                 bool progressed = false;
+                // Every barrier this pass may look at is tested at once: a test
+                // whose result is branched on costs the thread ~170 cycles, and
+                // tested one after another they delayed each issue by their
+                // sum (a result not needed this pass is not used).
+                const int ph_h = gu & 1;
+                const bool r_p = mbar_poll(aPfull + ph_h * 8, static_cast<uint32_t>(gu >> 1) & 1u);
+                const bool r_o = mbar_poll(aOempty, static_cast<uint32_t>(u_seg - 1) & 1u);
+                const bool r_full = mbar_poll(aFull + (s_slot % kStages) * 8, static_cast<uint32_t>(s_slot / kStages) & 1u);
+                const bool r_sfree = mbar_poll(aSfree, static_cast<uint32_t>(gs - 1) & 1u);
+                const bool r_q = mbar_poll(aQfull, static_cast<uint32_t>(s_seg) & 1u);
                 if (gu < 2 * gs) {
                     // O_half += P V_half for one unit: P from TMEM (8 columns per 16
                     // keys); V = the latent chunks of the tile's stage read N-major
                     // (64-dim blocks 8 KB apart, 16 keys = 2 KB per MMA).
                     const int h = gu & 1;
-                    const uint32_t t = static_cast<uint32_t>(gu >> 1);
                     const bool first = h == 0 && u_first;
                     const int u_stage = u_slot % kStages;
-                    if (mbar_poll(aPfull + h * 8, t & 1u) &&
-                        (!first || u_seg == 0 || mbar_poll(aOempty, static_cast<uint32_t>(u_seg - 1) & 1u))) {
+                    if (r_p && (!first || u_seg == 0 || r_o)) {
                         tc_fence_after_sync();
                         const uint64_t vd =
                             smem_desc_sw128(sKVa + u_stage * kStageBytes + h * (kBU * 128), kKvChunk, 1024);
@@ -482,10 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (gs < total) {
                     const int s_stage = s_slot % kStages;
-                    const uint32_t s_phase = static_cast<uint32_t>(s_slot / kStages) & 1u;
-                    if (mbar_poll(aFull + s_stage * 8, s_phase) &&
-                        (gs == 0 || mbar_poll(aSfree, static_cast<uint32_t>(gs - 1) & 1u)) &&
-                        (!s_first || mbar_poll(aQfull, static_cast<uint32_t>(s_seg) & 1u))) {
+                    if (r_full && (gs == 0 || r_sfree) && (!s_first || r_q)) {
                         tc_fence_after_sync();
                         // S_part = Q_part K_part^T: Q from TMEM (8 columns per 16 dims).
                         const uint64_t kvd = smem_desc_sw128(sKVa + s_stage * kStageBytes, 16, 1024);
