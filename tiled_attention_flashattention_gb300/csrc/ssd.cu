@@ -240,10 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t spins = 0;
             while (n_done < nch) {
                 bool any = false;
+                // The two barriers of each product are tested before either result
+                // is branched on (a branched-on test costs the thread ~170 cycles;
+                // these overlap).  Testing all seven every pass was slower.
                 if (n1 < nch) {
                     const int c = n1, u = c & 1;
-                    if (mbar_poll(smem_u32(&k.full[u]), (c >> 1) & 1) &&
-                        (c < 2 || mbar_poll(smem_u32(&k.g_free[u]), ((c - 2) >> 1) & 1))) {
+                    const bool r0 = mbar_poll(smem_u32(&k.full[u]), (c >> 1) & 1);
+                    const bool r1 = c < 2 || mbar_poll(smem_u32(&k.g_free[u]), ((c - 2) >> 1) & 1);
+                    if (r0 && r1) {
                         tc_fence_after_sync();
                         const uint32_t st = sb + u * kStageBytes;
                         const uint64_t ad = smem_desc_sw128(st + kOffC, 16, 1024);
@@ -260,8 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (n2 < n1) {
                     const int c = n2, u = c & 1;
-                    if (mbar_poll(smem_u32(&k.w_full[u]), (c >> 1) & 1) &&
-                        (c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1))) {
+                    const bool r0 = mbar_poll(smem_u32(&k.w_full[u]), (c >> 1) & 1);
+                    const bool r1 = c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1);
+                    if (r0 && r1) {
                         tc_fence_after_sync();
                         const uint64_t bd = smem_desc_sw128(sb + u * kStageBytes + kOffX, kAtom, 1024);
 #pragma unroll
@@ -290,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (n3 < n1) {
                     const int c = n3, u = c & 1;
-                    if (mbar_poll(smem_u32(&k.s_ready[u]), (c >> 1) & 1) &&
-                        (c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1))) {
+                    const bool r0 = mbar_poll(smem_u32(&k.s_ready[u]), (c >> 1) & 1);
+                    const bool r1 = c < 2 || mbar_poll(smem_u32(&k.y_free[u]), ((c - 2) >> 1) & 1);
+                    if (r0 && r1) {
                         tc_fence_after_sync();
                         const uint32_t st = sb + u * kStageBytes;
                         const uint64_t ad = smem_desc_sw128(st + kOffC, 16, 1024);
