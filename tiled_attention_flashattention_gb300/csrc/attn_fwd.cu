@@ -467,11 +467,14 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     }
                     const int iv = it++;
                     ATTN_TRACE(kAtWaitV, n);
-                    if (!(ok = mbar_wait(&c.full[islot(iv)], iphase(iv), ctl))) break;
+                    // V of tile n and P of tile n (one barrier per S buffer: the softmax
+                    // may already have finished tile n + 1, whose S was issued above),
+                    // both tested before either is waited for
+                    const bool v_seen = mbar_poll(smem_u32(&c.full[islot(iv)]), iphase(iv));
+                    const bool p_seen = mbar_poll(smem_u32(&c.p_full[n & 1]), static_cast<uint32_t>(n >> 1) & 1u);
+                    if (!v_seen && !(ok = mbar_wait(&c.full[islot(iv)], iphase(iv), ctl))) break;
                     ATTN_TRACE(kAtVSeen, n);
-                    // P of tile n: one barrier per S buffer (the softmax may already have
-                    // finished tile n + 1, whose S was issued above)
-                    if (!(ok = mbar_wait(&c.p_full[n & 1], static_cast<uint32_t>(n >> 1) & 1u, ctl))) break;
+                    if (!p_seen && !(ok = mbar_wait(&c.p_full[n & 1], static_cast<uint32_t>(n >> 1) & 1u, ctl))) break;
                     ATTN_TRACE(kAtP0Seen, n);
                     tc_fence_after_sync();
                     issue_PV(0, n & 1, islot(iv));
