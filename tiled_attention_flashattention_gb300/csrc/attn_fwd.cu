@@ -287,6 +287,27 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
         mbar_init(&c.drain, 1);
         c.abort = 0;
         fence_mbar_init();
+        if constexpr (!kSparse) {
+            // Dense forms: the Q tiles and K of the first key tile (ring item 0)
+            // leave before the block-wide setup sync, from the thread that
+            // initialised their barriers, which is also the TMA producer.  (The
+            // block-sparse form learns its first tile from the mask scan.)
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            if (p.inject != 1 && (has[0] || has[1])) {
+                mbar_arrive_expect_tx(&c.q_full, (has[0] + has[1]) * C::kQTileBytes);
+                for (int t = 0; t < 2; ++t)
+                    if (has[t])
+                        for (int ch = 0; ch < C::kChunks; ++ch)
+                            tma_load_3d(sQ + t * C::kQTileBytes + ch * kQChunkBytes, &tmQ, &c.q_full,
+                                        ch * 64, r0[t], bh);
+            }
+            if (lo < hi) {
+                mbar_arrive_expect_tx(&c.full[0], C::kKvTileBytes);
+                for (int ch = 0; ch < C::kChunks; ++ch)
+                    tma_load_3d(ring + ch * C::kKvChunkBytes, &tmK, &c.full[0], ch * 64, lo * BN, kvh);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, C::kTmemCols);
@@ -337,7 +358,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
             for (int t = 0; t < 2; ++t)
                 if (has[t]) qbytes += C::kQTileBytes;
             if (p.inject == 1) qbytes = 0;   // nothing ever completes q_full
-            if (qbytes) {
+            if (kSparse && qbytes) {          // (dense: issued at setup)
                 mbar_arrive_expect_tx(&c.q_full, qbytes);
                 for (int t = 0; t < 2; ++t)
                     if (has[t])
@@ -346,13 +367,14 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                                         ch * 64, r0[t], bh);
             }
             bool ok = true;
-            int it = 0;
+            int it = (!kSparse && first < hi) ? 1 : 0;     // ring items already issued
             if constexpr (kPipe) {
                 // The issuer's order over the key tiles the CTA computes (all of
                 // [first, hi), or the active ones of a block mask): K of the
                 // first, then for each tile the K of the next one (its S runs
                 // first) and the V of this one; the last tile has no next K.
-                int jk = first, jv = first;      // tiles of the next K and the next V to load
+                int jk = it ? next_any(first) : first;    // tiles of the next K and the next V to load
+                int jv = first;
                 bool k_turn = true;
                 while (jv < hi && ok) {
                     const bool kv = !(k_turn && jk < hi);
@@ -375,7 +397,17 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     k_turn = it == 1 ? true : !k_turn;
                 }
             } else {
-                for (int j = first; j < hi && ok; j = next_any(j)) {
+                int j = first;
+                if (it == 1) {
+                    // dense: K of the first tile is out; its V goes to item 1 (round 0)
+                    mbar_arrive_expect_tx(&c.full[1], C::kKvTileBytes);
+                    for (int ch = 0; ch < C::kChunks; ++ch)
+                        tma_load_3d(ring + C::kKvTileBytes + ch * C::kKvChunkBytes, &tmV, &c.full[1], ch * 64,
+                                    j * BN, kvh);
+                    it = 2;
+                    j = next_any(j);
+                }
+                for (; j < hi && ok; j = next_any(j)) {
                     for (int kv = 0; kv < 2; ++kv) {
                         const int slot = it % C::kSlots;
                         const uint32_t round = static_cast<uint32_t>(it / C::kSlots);
