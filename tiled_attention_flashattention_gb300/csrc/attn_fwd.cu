@@ -130,6 +130,7 @@ struct Params {
     int mask_qb, mask_kb;
     float c;            // scale * log2(e)
     int inject;         // 1: the producer never loads the Q tiles (tests the bounded waits)
+    int pf_stride;      // > 0: prefetch into L2 the Q tiles of block blockIdx.x + pf_stride
     int *status;
     uint64_t timeout_ns;
 };
@@ -419,6 +420,21 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                                         ch * 64, j * BN, kvh);
                         ++it;
                     }
+                }
+            }
+            // (one-tile forms only: in the two-tile form the extra producer code
+            // alone, never executed, cost the 16k causal shape 0.3 %)
+            if (kT == 1 && ok && p.pf_stride > 0 && blockIdx.x + p.pf_stride < gridDim.x) {
+                // The block that will most likely take this CTA's place on the SM
+                // (one wave of resident CTAs later): its Q tiles into L2 now, a few
+                // key tiles before this CTA ends, so its start does not wait on HBM.
+                const int b2 = static_cast<int>(blockIdx.x) + p.pf_stride;
+                const int bh2 = b2 % nbh;
+                const int qb2 = p.n_qblk - 1 - b2 / nbh;
+                for (int t = 0; t < kT; ++t) {
+                    const int rr = qb2 * (kT * kBM) + t * kBM;
+                    if (rr < p.N_q)
+                        for (int ch = 0; ch < C::kChunks; ++ch) tma_prefetch_l2_3d(&tmQ, ch * 64, rr, bh2);
                 }
             }
             if (!ok) {
@@ -909,6 +925,10 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         return 5;
     p.c = scale * 1.4426950408889634f;
     p.inject = env.inject;
+    // Q prefetch for the next block on an SM (one-tile forms, two CTAs per SM).
+    // Measured kernel-only: causal window 256 +2.4 %, causal 2k +1-2 %,
+    // block-sparse +0.4 %, symmetric window 256 unchanged.
+    p.pf_stride = kt == 1 ? 2 * env.num_sms : 0;
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
     const long long grid = static_cast<long long>(p.n_qblk) * B * H;
