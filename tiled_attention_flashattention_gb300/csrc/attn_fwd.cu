@@ -200,7 +200,10 @@ __device__ __forceinline__ Range kv_range(int r0, int r1, const Params &p)
     return {static_cast<int>(key_lo / BN), static_cast<int>((key_hi + BN - 1) / BN)};
 }
 
-template <int D, bool kSparse, int kT, int BN>
+// kPf: the CTA prefetches into L2 the Q tiles of the block that will take its
+// place on the SM (compiled in only where it is used: in the two-tile form the
+// extra producer code alone, never executed, cost the 16k causal MHA shape 0.3 %).
+template <int D, bool kSparse, int kT, int BN, bool kPf = (kT == 1)>
 __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMinBlocks)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -422,9 +425,7 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
                     }
                 }
             }
-            // (one-tile forms only: in the two-tile form the extra producer code
-            // alone, never executed, cost the 16k causal shape 0.3 %)
-            if (kT == 1 && ok && p.pf_stride > 0 && blockIdx.x + p.pf_stride < gridDim.x) {
+            if (kPf && ok && p.pf_stride > 0 && blockIdx.x + p.pf_stride < gridDim.x) {
                 // The block that will most likely take this CTA's place on the SM
                 // (one wave of resident CTAs later): its Q tiles into L2 now, a few
                 // key tiles before this CTA ends, so its start does not wait on HBM.
@@ -819,21 +820,21 @@ __global__ void __launch_bounds__(Cfg<D, kT, BN>::kThreads, Cfg<D, kT, BN>::kMin
     if (threadIdx.x == 0) ATTN_TRACE_CLOCK(1);
 }
 
-template <int D, bool kSparse, int kT, int BN = kBN>
+template <int D, bool kSparse, int kT, int BN = kBN, bool kPf = (kT == 1)>
 int launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
            const Params &p, int grid, const LaunchEnv &env, std::string &err)
 {
     static std::atomic<uint64_t> configured{0};   // one bit per device
     const size_t smem = smem_bytes<D, kT, BN>();
     {
-        cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(attn_fwd_kernel<D, kSparse, kT, BN>),
+        cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(attn_fwd_kernel<D, kSparse, kT, BN, kPf>),
                                             smem, configured);
         if (e != cudaSuccess) {
             err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
             return 5;
         }
     }
-    attn_fwd_kernel<D, kSparse, kT, BN><<<grid, Cfg<D, kT, BN>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
+    attn_fwd_kernel<D, kSparse, kT, BN, kPf><<<grid, Cfg<D, kT, BN>::kThreads, smem, env.stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("attn_fwd launch: ") + cudaGetErrorString(e);
@@ -925,10 +926,15 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
         return 5;
     p.c = scale * 1.4426950408889634f;
     p.inject = env.inject;
-    // Q prefetch for the next block on an SM (one-tile forms, two CTAs per SM).
-    // Measured kernel-only: causal window 256 +2.4 %, causal 2k +1-2 %,
-    // block-sparse +0.4 %, symmetric window 256 unchanged.
-    p.pf_stride = kt == 1 ? 2 * env.num_sms : 0;
+    // Q prefetch for the next block on an SM: in the one-tile forms (two CTAs
+    // per SM) and in the two-tile form for grouped heads, whose K / V mostly
+    // hit L2 already.  Measured kernel-only: causal window 256 +2.4 %, causal
+    // 2k +1-2 %, block-sparse +0.4 %, GQA 8k causal +1.4 %, symmetric window 256
+    // unchanged; in the two-tile form for MHA the 16k causal shape lost 0.2 %
+    // with it (its K / V prefixes already overflow L2).  (Not at d = 64, whose
+    // two-tile producer spills registers with the prefetch code.)
+    const bool pf2 = p.group > 1 && d == 128;
+    p.pf_stride = kt == 1 ? 2 * env.num_sms : (pf2 ? env.num_sms : 0);
     p.status = env.status;
     p.timeout_ns = env.timeout_ns;
     const long long grid = static_cast<long long>(p.n_qblk) * B * H;
@@ -946,6 +952,7 @@ int launch_attn_fwd(const void *Q, const void *K, const void *V, void *O, float 
     if (kt == 1)
         return d == 128 ? launch<128, false, 1, 64>(tq, tk, tv, to, p, g, env, err)
                         : launch<64, false, 1, 64>(tq, tk, tv, to, p, g, env, err);
+    if (pf2) return launch<128, false, 2, kBN, true>(tq, tk, tv, to, p, g, env, err);
     return d == 128 ? launch<128, false, 2>(tq, tk, tv, to, p, g, env, err)
                     : launch<64, false, 2>(tq, tk, tv, to, p, g, env, err);
 }
