@@ -11,6 +11,10 @@
 // How it maps to the GB300 SM, two-Q-tile form (one CTA per SM, 384 threads):
 //   warp 0       TMA producer: two Q tiles (2 x 128 rows) once, then K_j and
 //                V_j tiles into a ring of shared-memory slots (128-byte swizzle);
+//                its thread issues the Q tiles and the first K tile right after
+//                initialising the barriers, before the block's setup sync, and
+//                (kPf) prefetches into L2 the Q tiles of the block that will
+//                take this CTA's place on the SM;
 //   warp 1       tensor-core issuer: S_t = Q_t K_j^T into TMEM, then
 //                O_t += P_t V_j with P_t read from TMEM (it overwrites S_t);
 //   warps 4-7    softmax of Q tile 0 (one thread per row, TMEM lane = row);
