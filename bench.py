@@ -624,7 +624,9 @@ def run_ours(args, rank, world, local):
     buf_d = torch.empty(gb.mla_decode_host_device_bytes(dc.B, dc.H, dc.N_kv, dc.d_c, dc.d_r), dtype=torch.uint8,
                         device=dev)
     e2e_pre, e2e_dec = 0.0, 0.0
-    for k in range(e2e_steps + 1):
+    e2e_warm = max(3, args.warmup)      # the first calls also settle the host pipeline
+    pre_ms = []                          # per-step prefill e2e times (ms), for the spread
+    for k in range(e2e_steps + e2e_warm):
         flush.zero_()
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
@@ -634,7 +636,8 @@ def run_ours(args, rank, world, local):
         gb.mla_decode_host(*dec_p, scale=scale_d, O=Od_h, LSE=Ld_h, device_buf=buf_d)
         e2.record(stream)
         torch.cuda.synchronize()
-        if k > 0:
+        if k >= e2e_warm:
+            pre_ms.append(e0.elapsed_time(e1))
             e2e_pre += e0.elapsed_time(e1) / 1e3
             e2e_dec += e1.elapsed_time(e2) / 1e3
     gb.check()
@@ -687,7 +690,9 @@ def run_ours(args, rank, world, local):
                    "e2e": {"value": by_d * e2e_steps * world / e2e_dec / 1e9, "unit": "GB/s",
                            "h2d_bytes_per_step": h2d_d, "d2h_bytes_per_step": d2h_d}},
         "e2e": {"value": fl_p * e2e_steps * world / e2e_pre / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": d2h_p},
+                "h2d_bytes_per_step": h2d_p, "d2h_bytes_per_step": d2h_p,
+                "steps": e2e_steps, "warmup": e2e_warm,
+                "ms_per_step_min_median_max": [min(pre_ms), sorted(pre_ms)[len(pre_ms) // 2], max(pre_ms)]},
         "e2e_ceiling": {
             "what": "the e2e bytes of one step moved by plain pinned cudaMemcpyAsync (inputs in and results "
                     "out on two streams, no kernel), and the metric that copy time alone would allow",
